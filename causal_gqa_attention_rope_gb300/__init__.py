@@ -1,0 +1,252 @@
+"""Python binding of the GB300 attention library ``libna.so`` (C ABI in ``include/na.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libna.so``.  PyTorch supplies device memory and streams.  There is
+no CPU fallback: importing works without a GPU (so the symbols can be checked),
+but every compute call needs the built library and CUDA tensors, and raises
+otherwise.
+
+Entry points (same names as the C ABI):
+  na_rope_append_kv      fused qk-norm + RoPE + KV-cache append
+  na_attn_prefill_chunk  causal GQA attention of a chunk against the cache
+  na_attn_decode         single-token decode with per-key probabilities
+  na_prefill_workspace_size / na_decode_workspace_size / na_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libna.so")
+
+NA_OK = 0
+NA_ERR_INVALID_ARG = -1
+NA_ERR_UNSUPPORTED = -2
+NA_ERR_CAPACITY = -3
+NA_ERR_WORKSPACE = -4
+NA_ERR_CUDA = -5
+NA_ERR_DEVICE_TIMEOUT = -6
+
+NA_QK_NORM = 1
+NA_QK_NORM_ZERO_CENTERED = 2
+NA_V_NORM = 4
+NA_OUT_GATE = 8
+
+# Every symbol include/na.h declares.
+EXPORTED = ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
+            "na_prefill_workspace_size", "na_decode_workspace_size", "na_status_string")
+
+
+class na_attn_cfg(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("flags", ctypes.c_uint32)]
+
+
+class na_rope_params(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_double), ("yarn", ctypes.c_int32), ("factor", ctypes.c_double),
+                ("orig_max_pos", ctypes.c_int32), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double), ("attn_factor", ctypes.c_double)]
+
+
+class na_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("capacity", ctypes.c_int32)]
+
+
+class NAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {status_string(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libna.so (raises when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libna.so is not built ({path}); run __graft_entry__.build() or "
+                           f"python -m causal_gqa_attention_rope_gb300._build")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    cfgp = ctypes.POINTER(na_attn_cfg)
+    ropep = ctypes.POINTER(na_rope_params)
+    cachep = ctypes.POINTER(na_kv_cache)
+    lib.na_rope_append_kv.argtypes = [cfgp, ropep, I32, P, P, I32, P, P, P, P, P, P, cachep, P, P]
+    lib.na_attn_prefill_chunk.argtypes = [cfgp, I32, P, P, I32, I32, I32, P, cachep, P, P, P, SZ,
+                                          P, P]
+    lib.na_attn_decode.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, I32, P, SZ, P, P]
+    lib.na_prefill_workspace_size.argtypes = [cfgp, I32, I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.na_decode_workspace_size.argtypes = [cfgp, I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.na_status_string.argtypes = [ctypes.c_int]
+    lib.na_status_string.restype = ctypes.c_char_p
+    for name in ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
+                 "na_prefill_workspace_size", "na_decode_workspace_size"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().na_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------------ configuration --
+
+@dataclass
+class AttnConfig:
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    rotary_dim: Optional[int] = None
+    sm_scale: float = 0.0
+    rms_eps: float = 1e-6
+    qk_norm: bool = False
+    qk_norm_zero_centered: bool = False
+    v_norm: bool = False
+    out_gate: bool = False
+
+    @property
+    def flags(self) -> int:
+        return ((NA_QK_NORM if self.qk_norm else 0)
+                | (NA_QK_NORM_ZERO_CENTERED if self.qk_norm_zero_centered else 0)
+                | (NA_V_NORM if self.v_norm else 0) | (NA_OUT_GATE if self.out_gate else 0))
+
+    def c(self) -> na_attn_cfg:
+        rd = self.head_dim if self.rotary_dim is None else self.rotary_dim
+        return na_attn_cfg(self.num_heads, self.num_kv_heads, self.head_dim, rd, self.sm_scale,
+                           self.rms_eps, self.flags)
+
+
+@dataclass
+class RopeConfig:
+    base: float = 10000.0
+    yarn: bool = False
+    factor: float = 1.0
+    orig_max_pos: int = 0
+    beta_fast: float = 32.0
+    beta_slow: float = 1.0
+    attn_factor: float = 0.0
+
+    def c(self) -> na_rope_params:
+        return na_rope_params(self.base, int(self.yarn), self.factor, self.orig_max_pos,
+                              self.beta_fast, self.beta_slow, self.attn_factor)
+
+
+@dataclass
+class KVCache:
+    """Caller-owned bf16 cache tensors [batch, num_kv_heads, capacity, head_dim]."""
+    k: "object"
+    v: "object"
+
+    def c(self) -> na_kv_cache:
+        return na_kv_cache(_ptr(self.k), _ptr(self.v), int(self.k.shape[0]), int(self.k.shape[2]))
+
+
+# ---------------------------------------------------------------- helpers --
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libna operates on CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libna needs contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int):
+    if rc != NA_OK:
+        raise NAError(fn, rc)
+
+
+# ------------------------------------------------------------ entry points --
+
+def na_rope_append_kv(cfg: AttnConfig, rope: RopeConfig, cu_seqlens, cache_lens, q, k, v,
+                      q_out, cache: KVCache, q_norm_w=None, k_norm_w=None, status=None,
+                      total_tokens: Optional[int] = None, stream=None):
+    lib = load_library()
+    T = int(q.shape[0]) if total_tokens is None else int(total_tokens)
+    batch = int(cu_seqlens.numel()) - 1
+    c, r, kc = cfg.c(), rope.c(), cache.c()
+    rc = lib.na_rope_append_kv(ctypes.byref(c), ctypes.byref(r), batch, _ptr(cu_seqlens),
+                               _ptr(cache_lens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w),
+                               _ptr(k_norm_w), _ptr(q_out), ctypes.byref(kc), _ptr(status),
+                               _stream(stream))
+    _check("na_rope_append_kv", rc)
+
+
+def na_prefill_workspace_size(cfg: AttnConfig, batch: int, total_tokens: int, max_new_len: int,
+                              max_total_len: int) -> int:
+    lib = load_library()
+    out = ctypes.c_size_t(0)
+    c = cfg.c()
+    _check("na_prefill_workspace_size",
+           lib.na_prefill_workspace_size(ctypes.byref(c), batch, total_tokens, max_new_len,
+                                         max_total_len, ctypes.byref(out)))
+    return int(out.value)
+
+
+def na_decode_workspace_size(cfg: AttnConfig, batch: int, max_kv_len: int,
+                             num_splits: int = 0) -> int:
+    lib = load_library()
+    out = ctypes.c_size_t(0)
+    c = cfg.c()
+    _check("na_decode_workspace_size",
+           lib.na_decode_workspace_size(ctypes.byref(c), batch, max_kv_len, num_splits,
+                                        ctypes.byref(out)))
+    return int(out.value)
+
+
+def na_attn_prefill_chunk(cfg: AttnConfig, cu_seqlens, cache_lens, max_new_len: int,
+                          max_total_len: int, q_rot, cache: KVCache, out, gate=None,
+                          workspace=None, status=None, total_tokens: Optional[int] = None,
+                          stream=None):
+    lib = load_library()
+    T = int(q_rot.shape[0]) if total_tokens is None else int(total_tokens)
+    batch = int(cu_seqlens.numel()) - 1
+    c, kc = cfg.c(), cache.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(c), batch, _ptr(cu_seqlens), _ptr(cache_lens), T,
+                                   int(max_new_len), int(max_total_len), _ptr(q_rot),
+                                   ctypes.byref(kc), _ptr(gate), _ptr(out), _ptr(workspace),
+                                   ws_bytes, _ptr(status), _stream(stream))
+    _check("na_attn_prefill_chunk", rc)
+
+
+def na_attn_decode(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: int, out,
+                   probs=None, gate=None, workspace=None, num_splits: int = 0, status=None,
+                   stream=None):
+    lib = load_library()
+    batch = int(q_rot.shape[0])
+    c, kc = cfg.c(), cache.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    stride = int(probs.shape[-1]) if probs is not None else 0
+    rc = lib.na_attn_decode(ctypes.byref(c), batch, _ptr(q_rot), ctypes.byref(kc), _ptr(kv_lens),
+                            int(max_kv_len), _ptr(gate), _ptr(out), _ptr(probs), stride,
+                            int(num_splits), _ptr(workspace), ws_bytes, _ptr(status),
+                            _stream(stream))
+    _check("na_attn_decode", rc)
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A byte tensor usable as workspace (None when nbytes is 0)."""
+    import torch
+    if nbytes == 0:
+        return None
+    return torch.empty((nbytes + 15) // 16 * 16, dtype=torch.uint8, device=device)

@@ -1,0 +1,389 @@
+// na_api.cu -- C ABI of the attention library: argument validation, launch
+// planning (tile counts, KV splits, workspace layout) and kernel launches.
+// Nothing here allocates device memory or synchronises with the device.
+#include <math.h>
+#include <string.h>
+
+#include "na_internal.cuh"
+
+namespace {
+
+constexpr uint32_t kKnownFlags = NA_QK_NORM | NA_QK_NORM_ZERO_CENTERED | NA_V_NORM | NA_OUT_GATE;
+constexpr double kPi = 3.14159265358979323846;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cfg(const na_attn_cfg *c)
+{
+    if (!c)
+        return NA_ERR_INVALID_ARG;
+    if (c->num_heads <= 0 || c->num_kv_heads <= 0 || c->num_heads % c->num_kv_heads != 0)
+        return NA_ERR_INVALID_ARG;
+    if (c->rotary_dim < 0 || (c->rotary_dim & 1) || c->rotary_dim > c->head_dim)
+        return NA_ERR_INVALID_ARG;
+    if (c->flags & ~kKnownFlags)
+        return NA_ERR_INVALID_ARG;
+    if (!(c->rms_eps >= 0.f))
+        return NA_ERR_INVALID_ARG;
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return NA_ERR_UNSUPPORTED;
+    return NA_OK;
+}
+
+float score_scale_log2(const na_attn_cfg *c)
+{
+    const double s = c->sm_scale > 0.f ? (double)c->sm_scale : 1.0 / sqrt((double)c->head_dim);
+    return (float)(s * 1.4426950408889634);
+}
+
+int check_cache(const na_kv_cache *cache, int batch)
+{
+    if (!cache || !cache->k || !cache->v || cache->capacity <= 0 || cache->batch < batch)
+        return NA_ERR_INVALID_ARG;
+    if (!aligned16(cache->k) || !aligned16(cache->v))
+        return NA_ERR_INVALID_ARG;
+    return NA_OK;
+}
+
+int sm_count()
+{
+    static int cached = 0;
+    if (cached == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            cached = n;
+        else
+            return 148;
+    }
+    return cached;
+}
+
+// RoPE inverse frequencies in double (cortiq fns rope_inv_freq / yarn_inv_freq,
+// with the rotary dimension as the exponent's denominator).
+void rope_frequencies(const na_rope_params *r, int rd, double *out)
+{
+    const int half = rd / 2;
+    if (!r->yarn) {
+        for (int i = 0; i < half; i++)
+            out[i] = pow(r->base, -2.0 * i / rd);
+        return;
+    }
+    auto dim_at = [&](double rotations) {
+        return rd * log(r->orig_max_pos / (rotations * 2.0 * kPi)) / (2.0 * log(r->base));
+    };
+    const int low = (int)fmax(floor(dim_at(r->beta_fast)), 0.0);
+    const int high = (int)fmin(fmax(ceil(dim_at(r->beta_slow)), 0.0), (double)(half > 0 ? half - 1 : 0));
+    const double span = (double)(high > low + 1 ? high - low : 1);
+    for (int i = 0; i < half; i++) {
+        const double plain = pow(r->base, -2.0 * i / rd);
+        double ramp = (i > low ? i - low : 0) / span;
+        ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
+        // ramp 0: keep the plain frequency; ramp 1: divide it by the factor.
+        out[i] = plain * (1.0 - ramp) + (plain / r->factor) * ramp;
+    }
+}
+
+// Multiplier on cos and sin: given value, else 1, else YaRN's 0.1 ln(factor) + 1.
+double rope_attention_factor(const na_rope_params *r)
+{
+    if (r->attn_factor > 0.0)
+        return r->attn_factor;
+    if (r->yarn && r->factor > 1.0)
+        return 0.1 * log(r->factor) + 1.0;
+    return 1.0;
+}
+
+int check_rope(const na_rope_params *r)
+{
+    if (!r || !(r->base > 1.0))
+        return NA_ERR_INVALID_ARG;
+    if (r->yarn && (!(r->factor > 0.0) || r->orig_max_pos <= 0 || !(r->beta_fast > 0.0) ||
+                    !(r->beta_slow > 0.0)))
+        return NA_ERR_INVALID_ARG;
+    return NA_OK;
+}
+
+struct PrefillPlan {
+    int q_tiles, num_splits, split_len;
+    size_t ws_bytes;
+};
+
+// Split the keys across CTAs only when the (query tile, head, sequence) grid
+// would leave most SMs idle; the split count targets about four CTAs per SM.
+PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int max_new_len,
+                         int max_total_len)
+{
+    PrefillPlan pl{};
+    const int bm = prefill_q_tile(), bn = prefill_key_tile();
+    pl.q_tiles = (max_new_len + bm - 1) / bm;
+    const long long est = (long long)batch * pl.q_tiles * c->num_heads;
+    const long long target = 4ll * sm_count();
+    int splits = 1;
+    if (est < target && max_total_len > 2 * bn) {
+        splits = (int)((target + est - 1) / est);
+        const int max_by_len = (max_total_len + 2 * bn - 1) / (2 * bn);
+        splits = splits < max_by_len ? splits : max_by_len;
+        if (splits < 1)
+            splits = 1;
+    }
+    if (splits > 1) {
+        int len = (max_total_len + splits - 1) / splits;
+        len = (len + bn - 1) / bn * bn;
+        pl.split_len = len;
+        pl.num_splits = (max_total_len + len - 1) / len;
+    } else {
+        pl.split_len = max_total_len > 0 ? max_total_len : 1;
+        pl.num_splits = 1;
+    }
+    pl.ws_bytes = pl.num_splits > 1
+                      ? (size_t)total_tokens * c->num_heads * pl.num_splits * (c->head_dim + 2) * 4
+                      : 0;
+    return pl;
+}
+
+struct DecodePlan {
+    int split_len, max_splits, heads_per_cta;
+    size_t ws_bytes;
+};
+
+DecodePlan plan_decode(const na_attn_cfg *c, int batch, int max_kv_len, int num_splits)
+{
+    DecodePlan pl{};
+    const int tile = decode_key_tile();
+    const int group = c->num_heads / c->num_kv_heads;
+    pl.heads_per_cta = (group % 4 == 0) ? 4 : ((group % 2 == 0) ? 2 : 1);
+    const int len = max_kv_len > 0 ? max_kv_len : 1;
+    int split_len;
+    if (num_splits > 0) {
+        split_len = (len + num_splits - 1) / num_splits;
+    } else {
+        // Keys per unit: 512 by default; longer when the batch alone gives
+        // every SM several units.
+        const long long units_per_split = (long long)batch * c->num_kv_heads * (group / pl.heads_per_cta);
+        split_len = 512;
+        while (split_len < len && units_per_split * ((len + split_len - 1) / split_len) > 64ll * sm_count())
+            split_len *= 2;
+    }
+    split_len = (split_len + tile - 1) / tile * tile;
+    pl.split_len = split_len;
+    pl.max_splits = (len + split_len - 1) / split_len;
+    pl.ws_bytes = (size_t)batch * c->num_heads * pl.max_splits * (c->head_dim + 2) * 4;
+    return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *na_status_string(int status)
+{
+    switch (status) {
+    case NA_OK: return "ok";
+    case NA_ERR_INVALID_ARG: return "invalid argument";
+    case NA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case NA_ERR_CAPACITY: return "position beyond cache capacity or probability stride";
+    case NA_ERR_WORKSPACE: return "workspace missing or too small";
+    case NA_ERR_CUDA: return "CUDA runtime error";
+    case NA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_t batch,
+                      const int32_t *cu_seqlens, const int32_t *cache_lens, int32_t total_tokens,
+                      const void *q, const void *k, const void *v, const void *q_norm_w,
+                      const void *k_norm_w, void *q_out, const na_kv_cache *cache, int32_t *status,
+                      void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != NA_OK)
+        return rc;
+    if ((rc = check_rope(rope)) != NA_OK)
+        return rc;
+    if (batch <= 0 || total_tokens < 0)
+        return NA_ERR_INVALID_ARG;
+    if ((rc = check_cache(cache, batch)) != NA_OK)
+        return rc;
+    if (total_tokens == 0)
+        return NA_OK;
+    if (!cu_seqlens || !cache_lens || !q || !k || !v || !q_out)
+        return NA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out))
+        return NA_ERR_INVALID_ARG;
+    if ((cfg->flags & NA_QK_NORM) && (!q_norm_w || !k_norm_w))
+        return NA_ERR_INVALID_ARG;
+    if (rope_append_smem_bytes(cfg->num_heads, cfg->num_kv_heads, cfg->head_dim,
+                               cfg->rotary_dim) > 200 * 1024)
+        return NA_ERR_UNSUPPORTED;
+
+    double inv_freq[64];
+    rope_frequencies(rope, cfg->rotary_dim, inv_freq);
+    RopeAppendParams p{};
+    p.H = cfg->num_heads;
+    p.KV = cfg->num_kv_heads;
+    p.d = cfg->head_dim;
+    p.rd = cfg->rotary_dim;
+    p.flags = cfg->flags;
+    p.eps = cfg->rms_eps;
+    p.rope_scale = (float)rope_attention_factor(rope);
+    p.batch = batch;
+    p.capacity = cache->capacity;
+    p.total_tokens = total_tokens;
+    p.cu_seqlens = cu_seqlens;
+    p.cache_lens = cache_lens;
+    p.q = static_cast<const bf16 *>(q);
+    p.k = static_cast<const bf16 *>(k);
+    p.v = static_cast<const bf16 *>(v);
+    p.qw = static_cast<const bf16 *>(q_norm_w);
+    p.kw = static_cast<const bf16 *>(k_norm_w);
+    p.q_out = static_cast<bf16 *>(q_out);
+    p.cache_k = static_cast<bf16 *>(cache->k);
+    p.cache_v = static_cast<bf16 *>(cache->v);
+    p.status = status;
+    return launch_rope_append(p, inv_freq, cfg->rotary_dim / 2,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? NA_OK
+               : NA_ERR_CUDA;
+}
+
+int na_prefill_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t total_tokens,
+                              int32_t max_new_len, int32_t max_total_len, size_t *bytes)
+{
+    int rc = check_cfg(cfg);
+    if (rc != NA_OK)
+        return rc;
+    if (!bytes || batch <= 0 || total_tokens < 0 || max_new_len < 0 || max_total_len < 0)
+        return NA_ERR_INVALID_ARG;
+    *bytes = plan_prefill(cfg, batch, total_tokens, max_new_len, max_total_len).ws_bytes;
+    return NA_OK;
+}
+
+int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *cu_seqlens,
+                          const int32_t *cache_lens, int32_t total_tokens, int32_t max_new_len,
+                          int32_t max_total_len, const void *q_rot, const na_kv_cache *cache,
+                          const void *gate, void *out, void *workspace, size_t ws_bytes,
+                          int32_t *status, void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != NA_OK)
+        return rc;
+    if (batch <= 0 || total_tokens < 0 || max_new_len < 0 || max_total_len < 0)
+        return NA_ERR_INVALID_ARG;
+    if ((rc = check_cache(cache, batch)) != NA_OK)
+        return rc;
+    if (total_tokens == 0)
+        return NA_OK;
+    if (!cu_seqlens || !cache_lens || !q_rot || !out || max_new_len <= 0)
+        return NA_ERR_INVALID_ARG;
+    if (max_total_len > cache->capacity)
+        return NA_ERR_CAPACITY;
+    if (!aligned16(q_rot) || !aligned16(out))
+        return NA_ERR_INVALID_ARG;
+    const bool gated = (cfg->flags & NA_OUT_GATE) != 0;
+    if (gated && (!gate || !aligned16(gate)))
+        return NA_ERR_INVALID_ARG;
+    const PrefillPlan pl = plan_prefill(cfg, batch, total_tokens, max_new_len, max_total_len);
+    if (pl.ws_bytes > 0 && (!workspace || ws_bytes < pl.ws_bytes || !aligned16(workspace)))
+        return NA_ERR_WORKSPACE;
+
+    PrefillParams p{};
+    p.H = cfg->num_heads;
+    p.KV = cfg->num_kv_heads;
+    p.group = p.H / p.KV;
+    p.batch = batch;
+    p.capacity = cache->capacity;
+    p.scale_log2 = score_scale_log2(cfg);
+    p.max_new_len = max_new_len;
+    p.max_total_len = max_total_len;
+    p.q_tiles = pl.q_tiles;
+    p.split_len = pl.split_len;
+    p.num_splits = pl.num_splits;
+    p.flags = cfg->flags;
+    p.cu_seqlens = cu_seqlens;
+    p.cache_lens = cache_lens;
+    p.q = static_cast<const bf16 *>(q_rot);
+    p.cache_k = static_cast<const bf16 *>(cache->k);
+    p.cache_v = static_cast<const bf16 *>(cache->v);
+    p.gate = gated ? static_cast<const bf16 *>(gate) : nullptr;
+    p.out = static_cast<bf16 *>(out);
+    if (pl.ws_bytes > 0) {
+        p.part_o = static_cast<float *>(workspace);
+        p.part_ml = p.part_o + (size_t)total_tokens * p.H * pl.num_splits * cfg->head_dim;
+    }
+    p.status = status;
+    return launch_prefill(p, cfg->head_dim, total_tokens, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? NA_OK
+               : NA_ERR_CUDA;
+}
+
+int na_decode_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t max_kv_len,
+                             int32_t num_splits, size_t *bytes)
+{
+    int rc = check_cfg(cfg);
+    if (rc != NA_OK)
+        return rc;
+    if (!bytes || batch <= 0 || max_kv_len < 0 || num_splits < 0)
+        return NA_ERR_INVALID_ARG;
+    *bytes = plan_decode(cfg, batch, max_kv_len, num_splits).ws_bytes;
+    return NA_OK;
+}
+
+int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
+                   const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
+                   const void *gate, void *out, float *probs, int32_t probs_stride,
+                   int32_t num_splits, void *workspace, size_t ws_bytes, int32_t *status,
+                   void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != NA_OK)
+        return rc;
+    if (batch <= 0 || max_kv_len < 0 || num_splits < 0)
+        return NA_ERR_INVALID_ARG;
+    if ((rc = check_cache(cache, batch)) != NA_OK)
+        return rc;
+    if (!q_rot || !kv_lens || !out || !aligned16(q_rot) || !aligned16(out))
+        return NA_ERR_INVALID_ARG;
+    if (max_kv_len > cache->capacity)
+        return NA_ERR_CAPACITY;
+    if (probs && probs_stride < max_kv_len)
+        return NA_ERR_CAPACITY;
+    const bool gated = (cfg->flags & NA_OUT_GATE) != 0;
+    if (gated && !gate)
+        return NA_ERR_INVALID_ARG;
+    const DecodePlan pl = plan_decode(cfg, batch, max_kv_len, num_splits);
+    if (!workspace || ws_bytes < pl.ws_bytes || !aligned16(workspace))
+        return NA_ERR_WORKSPACE;
+
+    DecodeParams p{};
+    p.H = cfg->num_heads;
+    p.KV = cfg->num_kv_heads;
+    p.group = p.H / p.KV;
+    p.batch = batch;
+    p.capacity = cache->capacity;
+    p.scale_log2 = score_scale_log2(cfg);
+    p.split_len = pl.split_len;
+    p.max_splits = pl.max_splits;
+    p.head_chunks = p.group / pl.heads_per_cta;
+    p.total_units = batch * p.KV * p.head_chunks * pl.max_splits;
+    p.max_kv_len = max_kv_len;
+    p.flags = cfg->flags;
+    p.q = static_cast<const bf16 *>(q_rot);
+    p.cache_k = static_cast<const bf16 *>(cache->k);
+    p.cache_v = static_cast<const bf16 *>(cache->v);
+    p.gate = gated ? static_cast<const bf16 *>(gate) : nullptr;
+    p.kv_lens = kv_lens;
+    p.out = static_cast<bf16 *>(out);
+    p.probs = probs;
+    p.probs_stride = probs ? probs_stride : 0;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = p.part_o + (size_t)batch * p.H * pl.max_splits * cfg->head_dim;
+    p.status = status;
+    return launch_decode(p, cfg->head_dim, pl.heads_per_cta, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? NA_OK
+               : NA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+/*
+ * na.h -- C ABI of the GB300 (sm_103a) library for RoPE-rotated causal
+ * grouped-query attention over a per-sequence KV cache.
+ *
+ * The operation comes from two docs.rs source pages:
+ *   [cortiq]  cortiq-engine 0.5.39 src/attention.rs
+ *   [needle]  needle-core 0.3.1 src/v2/batch.rs
+ *
+ * Conventions shared by every entry point
+ *   - bf16 means IEEE bfloat16 stored as 16-bit words, little-endian.
+ *   - Token-packed tensors hold the new tokens of all sequences back to back
+ *     (varlen packing): token t belongs to sequence b when
+ *     cu_seqlens[b] <= t < cu_seqlens[b+1].
+ *   - The KV cache is head-major, one slot per absolute position:
+ *     k[b][kv_head][slot][head_dim] (same for v), slot = position.
+ *   - Every pointer argument is DEVICE memory unless its comment says HOST.
+ *     Configuration structs are HOST memory and are read only during the call.
+ *   - Ownership: the caller allocates and frees every buffer (including the
+ *     workspace).  The library allocates no device memory, never synchronises
+ *     the host with the device, and enqueues all work on `stream`
+ *     (a cudaStream_t; NULL is the legacy default stream).
+ *   - Errors: a negative na_status is returned when host-side validation fails;
+ *     nothing is enqueued in that case.  Conditions only the device can see
+ *     (a position past the cache capacity, an internal wait that timed out) are
+ *     reported by writing a nonzero na_status value into *status (a device
+ *     int32, may be NULL to skip reporting); the affected tile is skipped and the
+ *     kernel returns normally.  The library never clears *status: the caller
+ *     zeroes it and reads it when convenient.
+ *   - Alignment: q, k, v, q_out, gate, out and the cache base pointers must be
+ *     16-byte aligned, contiguous, with head_dim a multiple of 8.
+ */
+#ifndef NA_H
+#define NA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum na_status {
+    NA_OK = 0,
+    NA_ERR_INVALID_ARG = -1,   /* null pointer, bad size, num_heads % num_kv_heads != 0, ... */
+    NA_ERR_UNSUPPORTED = -2,   /* a shape or option this build does not implement */
+    NA_ERR_CAPACITY = -3,      /* a position does not fit the cache / probability stride */
+    NA_ERR_WORKSPACE = -4,     /* workspace missing or smaller than required */
+    NA_ERR_CUDA = -5,          /* a CUDA runtime call (launch, attribute) failed */
+    NA_ERR_DEVICE_TIMEOUT = -6 /* device only: a bounded wait inside a kernel gave up */
+} na_status;
+
+/* Option flags (na_attn_cfg.flags). */
+#define NA_QK_NORM 1u                 /* per-head RMSNorm of q and k before RoPE [cortiq fn rmsnorm_head] */
+#define NA_QK_NORM_ZERO_CENTERED 2u   /* with NA_QK_NORM: multiply by (1 + w) instead of w */
+#define NA_V_NORM 4u                  /* scale-less RMS of v before it enters the cache [cortiq fn vnorm_head] */
+#define NA_OUT_GATE 8u                /* out *= sigmoid(gate) after attention [cortiq fn apply_gate] */
+
+/* One attention layer [cortiq struct QwenAttnCfg, the in-scope fields]. */
+typedef struct na_attn_cfg {
+    int32_t num_heads;     /* H query heads */
+    int32_t num_kv_heads;  /* KV heads; H % KV == 0; query head h reads kv head h / (H / KV) */
+    int32_t head_dim;      /* d: 64 or 128 */
+    int32_t rotary_dim;    /* rd: even, 0 <= rd <= d; RoPE turns dims [0, rd) only */
+    float sm_scale;        /* score scale; <= 0 selects 1 / sqrt(head_dim) */
+    float rms_eps;         /* epsilon of the qk-norm and v-norm */
+    uint32_t flags;        /* NA_* option bits */
+} na_attn_cfg;
+
+/* RoPE frequencies [cortiq fns rope_inv_freq, yarn_inv_freq, rope_rotate_scaled]. */
+typedef struct na_rope_params {
+    double base;          /* inv_freq[i] = base^(-2 i / rd) */
+    int32_t yarn;         /* 0: plain RoPE; 1: YaRN ramp between extrapolation and interpolation */
+    double factor;        /* YaRN context extension factor (> 0) */
+    int32_t orig_max_pos; /* YaRN original_max_position_embeddings (> 0 when yarn) */
+    double beta_fast;     /* YaRN ramp bounds in rotations */
+    double beta_slow;
+    double attn_factor;   /* multiplier on cos and sin; <= 0 selects 1 without YaRN and
+                             0.1 ln(factor) + 1 with YaRN */
+} na_rope_params;
+
+/* Caller-owned per-sequence cache: k, v bf16 [batch][num_kv_heads][capacity][head_dim]. */
+typedef struct na_kv_cache {
+    void *k;
+    void *v;
+    int32_t batch;
+    int32_t capacity;
+} na_kv_cache;
+
+/*
+ * Fused qk-norm + RoPE + cache append for a chunk of new tokens.
+ * [cortiq fn finish_projection (norms before RoPE, partial rotary) and
+ *  fn rope_rotate_scaled; needle module doc "What has to stay sequential":
+ *  the chunk's K/V are written before any of its positions attends.]
+ *
+ * For new token t of sequence b, pos = cache_lens[b] + (t - cu_seqlens[b]):
+ *   q_out[t][h]            = RoPE(norm_q(q[t][h]), pos)         for every h
+ *   cache.k[b][g][pos]     = RoPE(norm_k(k[t][g]), pos)         for every g
+ *   cache.v[b][g][pos]     = vnorm(v[t][g])  (or v unchanged)
+ * RoPE turns pairs (x[i], x[i + rd/2]), i < rd/2, by pos * inv_freq[i] and
+ * multiplies both outputs by the attention factor.
+ *
+ *   cfg, rope     HOST structs.
+ *   batch         number of sequences (>= 1, <= cache->batch).
+ *   cu_seqlens    int32 [batch + 1], non-decreasing, cu_seqlens[0] == 0.
+ *   cache_lens    int32 [batch]: tokens already cached (prior length).
+ *   total_tokens  HOST copy of cu_seqlens[batch]; 0 is a no-op returning NA_OK.
+ *   q             bf16 [total_tokens][H][d];  k, v bf16 [total_tokens][KV][d].
+ *   q_norm_w, k_norm_w  bf16 [d] (shared by all heads), required with NA_QK_NORM, else ignored.
+ *   q_out         bf16 [total_tokens][H][d]: rotated queries (may not alias q).
+ *   status        device int32 or NULL; a token whose pos >= capacity is skipped and
+ *                 NA_ERR_CAPACITY is written.
+ * The caller advances cache_lens afterwards.
+ */
+int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_t batch,
+                      const int32_t *cu_seqlens, const int32_t *cache_lens,
+                      int32_t total_tokens, const void *q, const void *k, const void *v,
+                      const void *q_norm_w, const void *k_norm_w, void *q_out,
+                      const na_kv_cache *cache, int32_t *status, void *stream);
+
+/*
+ * Causal GQA attention of a chunk of new tokens against the cache.
+ * [cortiq fn qwen_attention_batch, portable batched attend: query bi of the
+ *  chunk sees keys 0 .. s0 + bi; fn attention_head: softmax(q.k * scale) . V;
+ *  fn apply_gate; needle fn batch_attention.]
+ *
+ * The chunk's keys must already be in the cache (na_rope_append_kv first).
+ * New token t of sequence b at pos = cache_lens[b] + (t - cu_seqlens[b]) and
+ * query head h attends keys 0 .. pos of kv head h / (H / KV):
+ *   out[t][h] = sum_j softmax_j(scale * q_rot[t][h] . k_j) v_j   (* sigmoid(gate[t][h]))
+ *
+ *   cache_lens    int32 [batch]: prior lengths (the same values given to na_rope_append_kv).
+ *   total_tokens  HOST copy of cu_seqlens[batch]; 0 is a no-op returning NA_OK.
+ *   max_new_len   HOST upper bound of cu_seqlens[b+1] - cu_seqlens[b].
+ *   max_total_len HOST upper bound of cache_lens[b] + new length; <= capacity.
+ *   q_rot         bf16 [total_tokens][H][d] (q_out of na_rope_append_kv).
+ *   gate          bf16 [total_tokens][H][d], required with NA_OUT_GATE, else ignored.
+ *   out           bf16 [total_tokens][H][d].
+ *   workspace     device scratch of at least na_prefill_workspace_size() bytes
+ *                 (NULL allowed when that size is 0).
+ */
+int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *cu_seqlens,
+                          const int32_t *cache_lens, int32_t total_tokens, int32_t max_new_len,
+                          int32_t max_total_len, const void *q_rot, const na_kv_cache *cache,
+                          const void *gate, void *out, void *workspace, size_t ws_bytes,
+                          int32_t *status, void *stream);
+
+/*
+ * Single-token decode with optional per-key probabilities.
+ * [cortiq fn attention_head (returns the per-key probabilities that feed
+ *  eviction scoring), fns qwen_attention_core and attend_all_heads: the current
+ *  token is appended first, then each group's K/V are streamed once for all its
+ *  query heads.]
+ *
+ *   q_rot      bf16 [batch][H][d], already rotated (one query per sequence).
+ *   kv_lens    int32 [batch]: keys to attend, current token included (0 gives a zero
+ *              output and writes no probabilities).
+ *   max_kv_len HOST upper bound of kv_lens; <= capacity and <= probs_stride.
+ *   gate       bf16 [batch][H][d] with NA_OUT_GATE, else ignored.
+ *   out        bf16 [batch][H][d].
+ *   probs      fp32 [batch][H][probs_stride] or NULL: probs[b][h][j] = p_j for
+ *              j < kv_lens[b]; entries past kv_lens[b] are not written.
+ *   num_splits KV splits per sequence (0 = choose automatically from the SM count).
+ *   workspace  at least na_decode_workspace_size() bytes.
+ */
+int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
+                   const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
+                   const void *gate, void *out, float *probs, int32_t probs_stride,
+                   int32_t num_splits, void *workspace, size_t ws_bytes, int32_t *status,
+                   void *stream);
+
+/* Workspace bytes (HOST out-parameter) that na_attn_prefill_chunk needs for these bounds. */
+int na_prefill_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t total_tokens,
+                              int32_t max_new_len, int32_t max_total_len, size_t *bytes);
+
+/* Workspace bytes (HOST out-parameter) that na_attn_decode needs for these bounds. */
+int na_decode_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t max_kv_len,
+                             int32_t num_splits, size_t *bytes);
+
+/* Static description of a status code (HOST string, never NULL). */
+const char *na_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NA_H */

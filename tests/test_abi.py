@@ -1,0 +1,147 @@
+"""The C ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and its host-side validation and planning answer correctly
+(no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_gqa_attention_rope_gb300 as na
+from causal_gqa_attention_rope_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return na.load_library()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "na.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(na_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert set(declared) >= {"na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode"}
+    for name in declared:
+        assert hasattr(lib, name), f"{name} missing from libna.so"
+    assert set(declared) == set(na.EXPORTED)
+
+
+def test_status_strings(lib):
+    assert na.status_string(0) == "ok"
+    for code in range(-6, 0):
+        assert na.status_string(code) not in ("", "unknown status")
+    assert na.status_string(-99) == "unknown status"
+
+
+def _cfg(**kw):
+    base = dict(num_heads=32, num_kv_heads=8, head_dim=128, rotary_dim=128)
+    base.update(kw)
+    return na.AttnConfig(**base).c()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_heads=30, num_kv_heads=8), na.NA_ERR_INVALID_ARG),
+    (dict(num_kv_heads=0), na.NA_ERR_INVALID_ARG),
+    (dict(rotary_dim=63), na.NA_ERR_INVALID_ARG),
+    (dict(rotary_dim=130), na.NA_ERR_INVALID_ARG),
+    (dict(head_dim=96, rotary_dim=96), na.NA_ERR_UNSUPPORTED),
+])
+def test_bad_config_rejected_before_launch(lib, kw, code):
+    c = _cfg(**kw)
+    out = ctypes.c_size_t(0)
+    assert lib.na_decode_workspace_size(ctypes.byref(c), 4, 100, 0, ctypes.byref(out)) == code
+
+
+def test_null_and_misaligned_buffers_rejected(lib):
+    c = _cfg()
+    cache = na.na_kv_cache(16, 16, 1, 64)  # fake non-null, aligned addresses
+    rc = lib.na_attn_decode(ctypes.byref(c), 1, None, ctypes.byref(cache), 16, 10, None, 16,
+                            None, 0, 0, 16, 1 << 20, None, None)
+    assert rc == na.NA_ERR_INVALID_ARG
+    rc = lib.na_attn_decode(ctypes.byref(c), 1, 18, ctypes.byref(cache), 16, 10, None, 16, None,
+                            0, 0, 16, 1 << 20, None, None)
+    assert rc == na.NA_ERR_INVALID_ARG  # q not 16-byte aligned
+    bad_cache = na.na_kv_cache(16, 24, 1, 64)
+    rc = lib.na_attn_decode(ctypes.byref(c), 1, 16, ctypes.byref(bad_cache), 16, 10, None, 16,
+                            None, 0, 0, 16, 1 << 20, None, None)
+    assert rc == na.NA_ERR_INVALID_ARG
+
+
+def test_capacity_and_workspace_checks(lib):
+    c = _cfg()
+    cache = na.na_kv_cache(16, 16, 2, 64)
+    # max_kv_len past capacity
+    rc = lib.na_attn_decode(ctypes.byref(c), 2, 16, ctypes.byref(cache), 16, 65, None, 16, None,
+                            0, 0, 16, 1 << 20, None, None)
+    assert rc == na.NA_ERR_CAPACITY
+    # probability stride shorter than the longest sequence
+    rc = lib.na_attn_decode(ctypes.byref(c), 2, 16, ctypes.byref(cache), 16, 40, None, 16, 16, 32,
+                            0, 16, 1 << 20, None, None)
+    assert rc == na.NA_ERR_CAPACITY
+    # workspace too small
+    rc = lib.na_attn_decode(ctypes.byref(c), 2, 16, ctypes.byref(cache), 16, 40, None, 16, None, 0,
+                            0, 16, 8, None, None)
+    assert rc == na.NA_ERR_WORKSPACE
+    # prefill: total length past capacity
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(c), 1, 16, 16, 10, 10, 65, 16,
+                                   ctypes.byref(cache), None, 16, None, 0, None, None)
+    assert rc == na.NA_ERR_CAPACITY
+    # batch larger than the cache's
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(c), 3, 16, 16, 10, 10, 20, 16,
+                                   ctypes.byref(cache), None, 16, None, 0, None, None)
+    assert rc == na.NA_ERR_INVALID_ARG
+    # gate required when the gate flag is set
+    cg = _cfg()
+    cg.flags = na.NA_OUT_GATE
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(cg), 1, 16, 16, 10, 10, 20, 16,
+                                   ctypes.byref(cache), None, 16, None, 1 << 30, None, None)
+    assert rc == na.NA_ERR_INVALID_ARG
+
+
+def test_rope_params_validated(lib):
+    c = _cfg()
+    cache = na.na_kv_cache(16, 16, 1, 64)
+    bad = na.na_rope_params(1.0, 0, 1.0, 0, 32.0, 1.0, 0.0)  # base must exceed 1
+    rc = lib.na_rope_append_kv(ctypes.byref(c), ctypes.byref(bad), 1, 16, 16, 4, 16, 16, 16, None,
+                               None, 16, ctypes.byref(cache), None, None)
+    assert rc == na.NA_ERR_INVALID_ARG
+    bad_yarn = na.na_rope_params(1e6, 1, 4.0, 0, 32.0, 1.0, 0.0)  # yarn needs orig_max_pos
+    rc = lib.na_rope_append_kv(ctypes.byref(c), ctypes.byref(bad_yarn), 1, 16, 16, 4, 16, 16, 16,
+                               None, None, 16, ctypes.byref(cache), None, None)
+    assert rc == na.NA_ERR_INVALID_ARG
+    qk = _cfg()
+    qk.flags = na.NA_QK_NORM
+    good = na.na_rope_params(1e4, 0, 1.0, 0, 32.0, 1.0, 0.0)
+    rc = lib.na_rope_append_kv(ctypes.byref(qk), ctypes.byref(good), 1, 16, 16, 4, 16, 16, 16,
+                               None, None, 16, ctypes.byref(cache), None, None)
+    assert rc == na.NA_ERR_INVALID_ARG  # norm weights required
+
+
+def test_zero_tokens_return_ok_without_launch(lib):
+    c = _cfg()
+    cache = na.na_kv_cache(16, 16, 1, 64)
+    good = na.na_rope_params(1e4, 0, 1.0, 0, 32.0, 1.0, 0.0)
+    assert lib.na_rope_append_kv(ctypes.byref(c), ctypes.byref(good), 1, None, None, 0, None, None,
+                                 None, None, None, None, ctypes.byref(cache), None, None) == 0
+    assert lib.na_attn_prefill_chunk(ctypes.byref(c), 1, None, None, 0, 0, 0, None,
+                                     ctypes.byref(cache), None, None, None, 0, None, None) == 0
+
+
+def test_workspace_sizes_follow_the_plan(lib):
+    # long chunks fill the GPU: no key split, no workspace
+    assert na.na_prefill_workspace_size(na.AttnConfig(40, 8, 128, 64), 1, 2048, 2048, 32768) == 0
+    # a short chunk with long history splits the keys: (d + 2) floats per split row
+    ws = na.na_prefill_workspace_size(na.AttnConfig(32, 8, 128), 1, 128, 128, 4096)
+    assert ws > 0 and ws % (128 * 32 * 130 * 4) == 0
+    # decode: one (d + 2)-float partial per (sequence, head, split)
+    ws = na.na_decode_workspace_size(na.AttnConfig(32, 8, 128), 64, 8192)
+    assert ws % (64 * 32 * 130 * 4) == 0 and ws >= 64 * 32 * 130 * 4
+    assert na.na_decode_workspace_size(na.AttnConfig(32, 8, 128), 64, 8192, 4) == \
+        64 * 32 * 4 * 130 * 4

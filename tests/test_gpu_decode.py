@@ -1,0 +1,96 @@
+"""Parity of split-KV decode (output and per-key probabilities) with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from harness import (assert_out_close, assert_probs_close, gpu_decode, oracle_flags, sample_rows,
+                     score_scale)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_decode(oracle, dec, rows_bh=None, stride=None):
+    s = dec.spec
+    return oracle.decode(s.H, s.KV, s.d, score_scale(s), oracle_flags(s), W.bf16_to_f64(dec.q),
+                         np.ascontiguousarray(W.bf16_to_f64(dec.cache_k)),
+                         np.ascontiguousarray(W.bf16_to_f64(dec.cache_v)), dec.kv_lens.numpy(),
+                         gate=W.bf16_to_f64(dec.gate), probs_stride=stride, rows_bh=rows_bh)
+
+
+def _check(oracle, dec, num_splits=0, with_probs=True):
+    s = dec.spec
+    out, probs, status = gpu_decode(dec, with_probs=with_probs, num_splits=num_splits)
+    assert status == 0
+    stride = probs.shape[-1] if probs is not None else None
+    ref_out, ref_p = _oracle_decode(oracle, dec, stride=stride)
+    assert_out_close(out.double().numpy(), ref_out, "decode out")
+    if with_probs:
+        lens = dec.kv_lens.tolist()
+        for b, n in enumerate(lens):
+            assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"probs b{b}")
+            assert bool((probs[b, :, n:] == -7.0).all()), "probs written past kv_len"
+
+
+SHAPES = {
+    "h32kv8d128": W.Spec(H=32, KV=8, d=128, rd=128),
+    "h4kv1d128_group4": W.Spec(H=4, KV=1, d=128, rd=128),
+    "h8kv8d64_mha": W.Spec(H=8, KV=8, d=64, rd=64),
+    "h10kv2d128_group5": W.Spec(H=10, KV=2, d=128, rd=128),
+    "h16kv2d64_group8_gate": W.Spec(H=16, KV=2, d=64, rd=64, out_gate=True),
+    "h4kv2d128_group2_scale": W.Spec(H=4, KV=2, d=128, rd=128, sm_scale=0.2),
+}
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_decode_edge_lengths(oracle, name):
+    dec = W.make_decode(SHAPES[name], [0, 1, 63, 64, 65, 700, 1500], 1536, seed=71)
+    _check(oracle, dec)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 17])
+def test_decode_forced_splits(oracle, splits):
+    dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128), [1200, 5, 999], 1280, seed=81)
+    _check(oracle, dec, num_splits=splits)
+
+
+def test_decode_without_probs(oracle):
+    dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128, out_gate=True), [300, 64], 512, seed=91)
+    _check(oracle, dec, with_probs=False)
+
+
+def test_decode_equals_last_prefill_row():
+    """Decode of the last token of a prefilled prompt equals that prefill row."""
+    from harness import gpu_chunked
+    wl = W.PrefillWorkload(name="t", spec=W.Spec(H=8, KV=2, d=128, rd=128), batch=1,
+                           prompt_len=300, chunk=300, capacity=512)
+    prompt = W.make_chunked_prompt(wl, seed=5)
+    out, q_rot, ck, cv, status = gpu_chunked(prompt)
+    assert status == 0
+    dec = W.DecodeInputs(spec=wl.spec, q=q_rot[:, -1].contiguous(), cache_k=ck, cache_v=cv,
+                         kv_lens=torch.tensor([300], dtype=torch.int32), gate=None)
+    d_out, _, st = gpu_decode(dec, with_probs=False)
+    assert st == 0
+    assert_out_close(d_out.double().numpy(), out[:, -1].double().numpy(), "decode vs prefill")
+
+
+def test_full_decode_b64_h32kv8_kv512to8192(oracle):
+    """Full-size decode workload: every output row's probabilities sum to 1,
+    and sampled (sequence, head) rows match the oracle in output and in every
+    per-key probability."""
+    dec = W.make_decode_workload(W.C3, seed=0)
+    out, probs, status = gpu_decode(dec)
+    assert status == 0
+    lens = dec.kv_lens.tolist()
+    B, H = dec.q.shape[0], dec.spec.H
+    for b in range(B):
+        n = lens[b]
+        mass = probs[b, :, :n].double().sum(-1)
+        assert torch.allclose(mass, torch.ones_like(mass), atol=1e-3), f"mass b{b}"
+        assert bool((probs[b, :, n:] == -7.0).all())
+    rows = sample_rows(B * H, 48, seed=13)
+    ref_out, ref_p = _oracle_decode(oracle, dec, rows_bh=rows, stride=probs.shape[-1])
+    for r in rows:
+        b, h = divmod(r, H)
+        assert_out_close(out[b, h].double().numpy(), ref_out[b, h], f"row {r}")
+        assert_probs_close(probs[b, h, :lens[b]].numpy(), ref_p[b, h, :lens[b]], f"probs {r}")

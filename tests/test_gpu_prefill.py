@@ -1,0 +1,158 @@
+"""Parity of the chunked causal GQA prefill (append + attend) with the oracle,
+from tiny ragged cases to the full-size workloads (sampled rows there)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from harness import (assert_out_close, check_cache, gpu_chunked, gpu_step, oracle_append,
+                     oracle_rows, prompt_as_step, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare_step(oracle, step, rows=None, what=""):
+    g = gpu_step(step)
+    assert g.status == 0, f"status {g.status}"
+    ost = oracle_append(oracle, step)
+    check_cache(g.cache_k, g.cache_v, step, ost)
+    T = step.total_tokens
+    rows = list(range(T)) if rows is None else rows
+    ref = oracle_rows(oracle, step, ost, rows)
+    got = g.out[rows].to(torch.float64).numpy()
+    return assert_out_close(got, ref, what)
+
+
+def test_prefill_h4kv2d64_single_chunk_all_rows(oracle):
+    """128-token prompt, one chunk, empty cache, 4/2 heads, d 64, base 1e4."""
+    prompt = W.make_chunked_prompt(W.C1, seed=0)
+    step = prompt_as_step(prompt)
+    _compare_step(oracle, step, what="h4kv2d64 t128")
+
+
+RAGGED = {
+    "t1_empty_cache": ([0], [1]),
+    "t3_prior77": ([77], [3]),
+    "t127": ([0], [127]),
+    "t129_prior5": ([5], [129]),
+    "t200_prior300": ([300], [200]),
+}
+
+
+@pytest.mark.parametrize("name", list(RAGGED))
+def test_prefill_ragged_lengths(oracle, name):
+    prior, new = RAGGED[name]
+    spec = W.Spec(H=8, KV=2, d=128, rd=128, rope=W.RopeParams(base=5e5), std=0.5)
+    step = W.make_step(spec, prior, new, 512, seed=21)
+    _compare_step(oracle, step, what=name)
+
+
+SHAPES = {
+    "group5_d128_partial_yarn": W.Spec(H=10, KV=2, d=128, rd=64,
+                                        rope=W.RopeParams(base=1e6, yarn=True, factor=4.0,
+                                                          orig_max_pos=8192)),
+    "group8_d64": W.Spec(H=8, KV=1, d=64, rd=64, rope=W.RopeParams(base=1e4)),
+    "mha_d64_qknorm_gate_vnorm": W.Spec(H=3, KV=3, d=64, rd=64, qk_norm=True, v_norm=True,
+                                         out_gate=True),
+    "group16_qknorm_gate": W.Spec(H=32, KV=2, d=128, rd=128, rope=W.RopeParams(base=1e6),
+                                   qk_norm=True, out_gate=True),
+    "explicit_scale": W.Spec(H=4, KV=2, d=128, rd=128, sm_scale=0.05),
+}
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_prefill_shapes_varlen(oracle, name):
+    spec = SHAPES[name]
+    step = W.make_step(spec, [0, 250, 31], [70, 1, 140], 512, seed=31)
+    _compare_step(oracle, step, what=name)
+
+
+def test_prefill_short_chunk_long_history_splits_keys(oracle):
+    """Few query rows against a long history: the launch splits the keys and
+    merges the partials."""
+    spec = W.Spec(H=4, KV=1, d=128, rd=128, rope=W.RopeParams(base=5e5))
+    step = W.make_step(spec, [3000], [16], 4096, seed=41)
+    _compare_step(oracle, step, what="split keys")
+
+
+def test_prefill_varlen_small_all_rows(oracle):
+    """Packed varlen step with qk-norm and gate (the mixed-serving options) at
+    a size the oracle checks in full."""
+    spec = W.C5.spec
+    step = W.make_step(spec, [0, 300, 1024, 77], [130, 1, 65, 200], 1536, seed=51)
+    _compare_step(oracle, step, what="varlen small")
+
+
+def test_chunked_equals_single_chunk_on_gpu():
+    """The same prompt in 4 chunks of 64 and in one chunk of 256 gives the same
+    outputs (within the output tolerance) and the same cache bits."""
+    wl = W.PrefillWorkload(name="t", spec=W.Spec(H=8, KV=2, d=128, rd=128,
+                                                 rope=W.RopeParams(base=5e5), std=0.5),
+                           batch=2, prompt_len=256, chunk=64, capacity=512)
+    p4 = W.make_chunked_prompt(wl, seed=61)
+    p1 = W.make_chunked_prompt(W.PrefillWorkload(**{**wl.__dict__, "chunk": 256}), seed=61)
+    o4, _, k4, v4, s4 = gpu_chunked(p4)
+    o1, _, k1, v1, s1 = gpu_chunked(p1)
+    assert s4 == 0 and s1 == 0
+    assert torch.equal(k4.view(torch.int16), k1.view(torch.int16))
+    assert torch.equal(v4.view(torch.int16), v1.view(torch.int16))
+    assert_out_close(o4.double().numpy(), o1.double().numpy(), "chunked vs single")
+
+
+def test_empty_chunk_is_noop():
+    import causal_gqa_attention_rope_gb300 as na
+    from harness import attn_cfg
+    spec = W.Spec(H=4, KV=2, d=64, rd=64)
+    dev = "cuda"
+    k = W.sentinel_fill((1, 2, 8, 64)).to(dev)
+    cache = na.KVCache(k, k.clone())
+    e = torch.empty(0, 4, 64, dtype=torch.bfloat16, device=dev)
+    na.na_attn_prefill_chunk(attn_cfg(spec), torch.zeros(2, dtype=torch.int32, device=dev),
+                             torch.zeros(1, dtype=torch.int32, device=dev), 0, 0, e, cache, e,
+                             total_tokens=0)
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------- full-size workloads --
+
+def _chunked_full(oracle, wl, n_rows, seed=0):
+    prompt = W.make_chunked_prompt(wl, seed=seed)
+    out, q_rot, ck, cv, status = gpu_chunked(prompt)
+    assert status == 0
+    step = prompt_as_step(prompt)
+    ost = oracle_append(oracle, step)
+    # cache of the whole prompt: every slot within 1 ulp, the rest untouched
+    from harness import assert_within_ulp
+    L = prompt.prompt_len
+    assert_within_ulp(ck[:, :, :L], ost.cache_k[:, :, :L], "cache K (full prompt)")
+    assert np.array_equal(cv[:, :, :L].double().numpy(), ost.cache_v[:, :, :L])
+    assert bool((ck[:, :, L:].contiguous().view(torch.int16) == W.SENTINEL_BITS).all())
+    # sampled rows: first and last row of every chunk plus seeded random rows
+    rows = set()
+    for c in range(prompt.num_chunks):
+        lo, hi = prompt.chunk_bounds(c)
+        rows.update((lo, hi - 1))
+    rows.update(sample_rows(L, n_rows, seed=7))
+    rows = sorted(rows)
+    ref = oracle_rows(oracle, step, ost, rows)
+    got = out[0, rows].double().numpy()
+    return assert_out_close(got, ref, wl.name)
+
+
+def test_full_chunked_prefill_h32kv8_t4096_chunk128(oracle):
+    _chunked_full(oracle, W.C2, n_rows=24)
+
+
+def test_full_yarn_prefill_h40kv8_rd64_t32768_chunk2048(oracle):
+    _chunked_full(oracle, W.C4, n_rows=6)
+
+
+def test_full_varlen_step_b16_qknorm_gate(oracle):
+    step = W.make_varlen_step(W.C5, seed=0)
+    rows = sample_rows(step.total_tokens, 40, seed=9)
+    # also the first and last new token of every sequence
+    cu = step.cu_seqlens.tolist()
+    for b in range(step.batch):
+        if cu[b + 1] > cu[b]:
+            rows += [cu[b], cu[b + 1] - 1]
+    _compare_step(oracle, step, rows=sorted(set(rows)), what="varlen full")
