@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--only", choices=["chunked", "decode", "varlen", "yarn"], default=None,
+                    help="time one workload and print its record (profiling runs)")
     return ap.parse_args()
 
 
@@ -498,7 +500,7 @@ def cpu_baseline_chunked(wl: W.PrefillWorkload, budget_s: float):
     rows, spent, flops = [], 0.0, 0.0
     order = np.linspace(0, L - 1, 64).astype(int).tolist()
     i = 0
-    while spent < budget_s and i < len(order) * 4:
+    while spent < budget_s and i < len(order) * 64:
         r = order[i % len(order)] if i < len(order) else int(np.random.default_rng(i).integers(L))
         t0 = time.perf_counter()
         oracle_rows(o, step, ost, [r])
@@ -554,6 +556,15 @@ def main():
     na.load_library()
     peaks = load_peaks()
     flush = Flusher()
+    if args.only:
+        fn = {"chunked": lambda: bench_chunked(W.C2, args.steps, args.warmup, peaks, flush, False),
+              "decode": lambda: bench_decode(W.C3, args.steps, args.warmup, peaks, flush),
+              "varlen": lambda: bench_varlen(W.C5, args.steps, args.warmup, peaks, flush),
+              "yarn": lambda: bench_chunked(W.C4, args.steps, args.warmup, peaks, flush, False)}
+        rec = fn[args.only]()
+        if rank == 0:
+            print(json.dumps(dict(rec, only=args.only)))
+        return
     sampler = ClockSampler()
     sampler.start()
     barrier(world)

@@ -12,12 +12,20 @@
 // One CTA per token.  The token's H + 2 KV rows (a few KB, contiguous in q, k
 // and v) are read with 16-byte loads, staged in shared memory as fp32, normed
 // and rotated by one warp per row, and written back with 16-byte stores: q_out
-// contiguously, K and V into their head-major cache slots.  The angle table is
-// computed once per token and shared by all heads: the angle pos * inv_freq[i]
-// is formed in double, reduced by whole turns in double (exact to ~1e-12 rad
-// for positions up to 2^31 and frequencies <= 1), and only the reduced angle in
-// [-pi, pi] goes through single-precision sincosf.  The kernel is bound by HBM
-// traffic: 2 * (H + 2 KV) * d * 2 bytes per token.
+// contiguously, K and V into their head-major cache slots.  The kernel is bound
+// by HBM traffic: 2 * (H + 2 KV) * d * 2 bytes per token.
+//
+// Precision.  The stored bf16 value is the correctly rounded result of the
+// exact rotation in all but vanishing cases, also where x0 cos - x1 sin nearly
+// cancels: the angle pos * inv_freq[i] is formed and reduced by whole turns in
+// double, its cos and sin come from double sincos (once per token and pair
+// index, shared by all heads) and are split into fp32 hi + lo parts; the
+// rotation is evaluated with error-free fp32 products (fmaf residuals) and an
+// error-free sum, so its absolute error is ~2^-44 of the operands.  The norm
+// weight enters as the exact product x * w of two bf16 values (for the
+// zero-centred style, x + x * w is kept as an fp32 hi + lo pair), and the row
+// factors (1 / rms, and the attention factor on the rotated dims) are applied
+// last as one relative rounding.
 #include "na_internal.cuh"
 
 namespace {
@@ -28,6 +36,40 @@ struct RopeTable {
 
 constexpr int kThreads = 256;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+// a = x * w as an unevaluated fp32 sum hi + lo (exact).
+struct F2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ F2 weighted(float x, float w, bool zero_centered)
+{
+    const float p = x * w;
+    const float pe = fmaf(x, w, -p);  // exact residual of the product
+    if (!zero_centered)
+        return {p, pe};
+    // x * (1 + w) = x + x * w: error-free sum of x and p, residuals folded into lo
+    const float s = x + p;
+    const float bb = s - x;
+    const float se = (x - (s - bb)) + (p - bb);
+    return {s, se + pe};
+}
+
+// u * c + v * d with u, v as hi + lo pairs and c, d as hi + lo pairs, returned
+// as hi + lo.  Leading products are exact (fmaf residuals); the leading sum is
+// error-free; the cross terms are small and rounded once.
+__device__ __forceinline__ F2 dot2(F2 u, float ch, float cl, F2 v, float dh, float dl)
+{
+    const float p0 = u.hi * ch;
+    const float e0 = fmaf(u.hi, ch, -p0);
+    const float p1 = v.hi * dh;
+    const float e1 = fmaf(v.hi, dh, -p1);
+    const float s = p0 + p1;
+    const float bb = s - p0;
+    const float t = (p0 - (s - bb)) + (p1 - bb);
+    const float cross = fmaf(u.hi, cl, fmaf(u.lo, ch, fmaf(v.hi, dl, v.lo * dh)));
+    return {s, t + (e0 + e1) + cross};
+}
 
 __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendParams p,
                                                                const RopeTable tab)
@@ -54,16 +96,16 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendP
         return;
     }
 
-    float *xs = smem_f;                                      // [rows][d]
-    float2 *cs = reinterpret_cast<float2 *>(smem_f + rows * d);  // [half] (cos, sin) * scale
+    float *xs = smem_f;                                          // [rows][d]
+    float4 *cs = reinterpret_cast<float4 *>(smem_f + rows * d);  // [half] (cos hi, cos lo, sin hi, sin lo)
 
     for (int i = threadIdx.x; i < half; i += kThreads) {
         const double angle = (double)pos * tab.inv_freq[i];
-        const double turns = rint(angle * (1.0 / kTwoPi));
-        const float r = (float)fma(-turns, kTwoPi, angle);
-        float s, c;
-        sincosf(r, &s, &c);
-        cs[i] = make_float2(c * p.rope_scale, s * p.rope_scale);
+        const double r = fma(-rint(angle * (1.0 / kTwoPi)), kTwoPi, angle);
+        double sd, cd;
+        sincos(r, &sd, &cd);
+        const float ch = (float)cd, sh = (float)sd;
+        cs[i] = make_float4(ch, (float)(cd - (double)ch), sh, (float)(sd - (double)sh));
     }
 
     const int cpr = d / 8;  // 16-byte chunks per row
@@ -93,35 +135,40 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendP
         float *x = xs + r * d;
         const bool is_v = r >= H + KV;
         const bool normed = is_v ? v_norm : qk_norm;
+        float f = 1.0f;  // row factor (1 / rms), applied last
         if (normed) {
-            float ss = 0.f;
+            float ss = 0.f;  // squares of bf16 values are exact in fp32
             for (int i = lane; i < d; i += 32)
-                ss += x[i] * x[i];
+                ss = fmaf(x[i], x[i], ss);
 #pragma unroll
             for (int o = 16; o; o >>= 1)
                 ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = 1.0f / sqrtf(ss / (float)d + p.eps);
-            if (is_v) {
-                for (int i = lane; i < d; i += 32)
-                    x[i] *= inv;
-            } else {
-                const bf16 *w = r < H ? p.qw : p.kw;
-                for (int i = lane; i < d; i += 32) {
-                    float wi = __bfloat162float(w[i]);
-                    if (zero_centered)
-                        wi += 1.0f;
-                    x[i] = x[i] * inv * wi;
-                }
-            }
-            __syncwarp();
+            f = 1.0f / sqrtf(ss / (float)d + p.eps);
         }
-        if (!is_v) {
-            for (int i = lane; i < half; i += 32) {
-                const float2 c = cs[i];
-                const float x0 = x[i], x1 = x[i + half];
-                x[i] = x0 * c.x - x1 * c.y;
-                x[i + half] = x0 * c.y + x1 * c.x;
-            }
+        if (is_v) {
+            for (int i = lane; i < d; i += 32)
+                x[i] *= f;
+            continue;
+        }
+        const bf16 *wp = normed ? (r < H ? p.qw : p.kw) : nullptr;
+        auto a_of = [&](int i) -> F2 {
+            if (!wp)
+                return {x[i], 0.f};
+            return weighted(x[i], __bfloat162float(wp[i]), zero_centered);
+        };
+        const float fr = f * p.rope_scale;  // the attention factor scales rotated dims only
+        for (int i = lane; i < half; i += 32) {
+            const float4 c = cs[i];
+            const F2 a0 = a_of(i), a1 = a_of(i + half);
+            const F2 neg_a1 = {-a1.hi, -a1.lo};
+            const F2 y0 = dot2(a0, c.x, c.y, neg_a1, c.z, c.w);  // a0 cos - a1 sin
+            const F2 y1 = dot2(a0, c.z, c.w, a1, c.x, c.y);      // a0 sin + a1 cos
+            x[i] = fmaf(y0.hi, fr, y0.lo * fr);
+            x[i + half] = fmaf(y1.hi, fr, y1.lo * fr);
+        }
+        for (int i = p.rd + lane; i < d; i += 32) {
+            const F2 a = a_of(i);
+            x[i] = fmaf(a.hi, f, a.lo * f);
         }
     }
     __syncthreads();
@@ -148,7 +195,7 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq
     RopeTable tab;
     for (int i = 0; i < 64; i++)
         tab.inv_freq[i] = i < half ? inv_freq[i] : 0.0;
-    const size_t smem = ((size_t)(p.H + 2 * p.KV) * p.d + 2 * (size_t)half) * sizeof(float);
+    const size_t smem = rope_append_smem_bytes(p.H, p.KV, p.d, p.rd);
     static size_t configured = 0;
     if (smem > 48 * 1024 && smem > configured) {
         cudaError_t e = cudaFuncSetAttribute(rope_append_kernel,
@@ -164,5 +211,5 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq
 
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd)
 {
-    return ((size_t)(H + 2 * KV) * d + 2 * (size_t)(rd / 2)) * sizeof(float);
+    return ((size_t)(H + 2 * KV) * d + 4 * (size_t)(rd / 2)) * sizeof(float);
 }
