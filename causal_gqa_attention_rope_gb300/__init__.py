@@ -37,7 +37,8 @@ NA_OUT_GATE = 8
 
 # Every symbol include/na.h declares.
 EXPORTED = ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
-            "na_prefill_workspace_size", "na_decode_workspace_size", "na_status_string")
+            "na_attn_decode_static_ws", "na_prefill_workspace_size", "na_decode_workspace_size",
+            "na_status_string")
 
 
 class na_attn_cfg(ctypes.Structure):
@@ -84,12 +85,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.na_attn_prefill_chunk.argtypes = [cfgp, I32, P, P, I32, I32, I32, P, cachep, P, P, P, SZ,
                                           P, P]
     lib.na_attn_decode.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, I32, P, SZ, P, P]
+    lib.na_attn_decode_static_ws.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, I32, P,
+                                             P]
     lib.na_prefill_workspace_size.argtypes = [cfgp, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_decode_workspace_size.argtypes = [cfgp, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_status_string.argtypes = [ctypes.c_int]
     lib.na_status_string.restype = ctypes.c_char_p
     for name in ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
-                 "na_prefill_workspace_size", "na_decode_workspace_size"):
+                 "na_attn_decode_static_ws", "na_prefill_workspace_size",
+                 "na_decode_workspace_size"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -242,6 +246,23 @@ def na_attn_decode(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: 
                             int(num_splits), _ptr(workspace), ws_bytes, _ptr(status),
                             _stream(stream))
     _check("na_attn_decode", rc)
+
+
+def na_attn_decode_static_ws(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: int,
+                             out, probs=None, gate=None, num_splits: int = 0, status=None,
+                             stream=None):
+    """na_attn_decode without a workspace argument: the split partials live in
+    a fixed 20 MiB device array inside the library, for callers that cannot
+    allocate device memory.  Calls that overlap on the GPU race on that array."""
+    lib = load_library()
+    batch = int(q_rot.shape[0])
+    c, kc = cfg.c(), cache.c()
+    stride = int(probs.shape[-1]) if probs is not None else 0
+    rc = lib.na_attn_decode_static_ws(ctypes.byref(c), batch, _ptr(q_rot), ctypes.byref(kc),
+                                      _ptr(kv_lens), int(max_kv_len), _ptr(gate), _ptr(out),
+                                      _ptr(probs), stride, int(num_splits), _ptr(status),
+                                      _stream(stream))
+    _check("na_attn_decode_static_ws", rc)
 
 
 def workspace(nbytes: int, device="cuda"):

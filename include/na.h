@@ -168,6 +168,34 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
                    int32_t num_splits, void *workspace, size_t ws_bytes, int32_t *status,
                    void *stream);
 
+/*
+ * na_attn_decode for callers that cannot supply a workspace.
+ * (An addition of this library; the pages have no counterpart.)
+ *
+ * Some callers have no way to allocate device memory for the workspace: a
+ * plugin inside another runtime that owns all device memory and exposes no
+ * allocator, or a serving loop that may not allocate once it is running.  This
+ * entry point takes the same arguments as na_attn_decode minus the workspace
+ * and keeps the split partials in a fixed 20 MiB device array inside the
+ * library, so the call allocates nothing.  That array exists on every GPU that
+ * loads the library, for as long as the library stays loaded.
+ *
+ *   - Sizes whose na_decode_workspace_size() exceeds 20 MiB are rejected with
+ *     NA_ERR_WORKSPACE before anything is enqueued (for 32 query heads and
+ *     head_dim 128: batch * max_kv_len up to about 640K keys with the automatic
+ *     split choice).
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents; the
+ *     decode needs nothing in it to start at zero.  Calls whose kernels overlap
+ *     on the GPU (other streams, other host threads) race on the array: order
+ *     them on one stream.
+ */
+int na_attn_decode_static_ws(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
+                             const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
+                             const void *gate, void *out, float *probs, int32_t probs_stride,
+                             int32_t num_splits, int32_t *status, void *stream);
+
 /* Workspace bytes (HOST out-parameter) that na_attn_prefill_chunk needs for these bounds. */
 int na_prefill_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t total_tokens,
                               int32_t max_new_len, int32_t max_total_len, size_t *bytes);
