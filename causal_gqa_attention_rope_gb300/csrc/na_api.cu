@@ -110,7 +110,8 @@ struct PrefillPlan {
 };
 
 // Split the keys across CTAs only when the (query tile, head, sequence) grid
-// would leave most SMs idle; the split count targets about four CTAs per SM.
+// would leave most SMs idle (one CTA owns an SM); the split count targets about
+// two CTAs per SM, each split covering at least two key tiles.
 PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int max_new_len,
                          int max_total_len)
 {
@@ -118,7 +119,7 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     const int bm = prefill_q_tile(), bn = prefill_key_tile();
     pl.q_tiles = (max_new_len + bm - 1) / bm;
     const long long est = (long long)batch * pl.q_tiles * c->num_heads;
-    const long long target = 4ll * sm_count();
+    const long long target = 2ll * sm_count();
     int splits = 1;
     if (est < target && max_total_len > 2 * bn) {
         splits = (int)((target + est - 1) / est);
@@ -278,6 +279,9 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
         return NA_ERR_INVALID_ARG;
     if (max_total_len > cache->capacity)
         return NA_ERR_CAPACITY;
+    if ((long long)cache->batch * cfg->num_kv_heads * cache->capacity >= (1ll << 31) ||
+        (long long)total_tokens * cfg->num_heads * cfg->head_dim >= (1ll << 40))
+        return NA_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
     if (!aligned16(q_rot) || !aligned16(out))
         return NA_ERR_INVALID_ARG;
     const bool gated = (cfg->flags & NA_OUT_GATE) != 0;
@@ -312,7 +316,8 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
         p.part_ml = p.part_o + (size_t)total_tokens * p.H * pl.num_splits * cfg->head_dim;
     }
     p.status = status;
-    return launch_prefill(p, cfg->head_dim, total_tokens, static_cast<cudaStream_t>(stream)) ==
+    return launch_prefill(p, cfg->head_dim, total_tokens, cache->batch,
+                          static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? NA_OK
                : NA_ERR_CUDA;

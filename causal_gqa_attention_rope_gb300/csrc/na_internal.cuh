@@ -204,7 +204,8 @@ struct PrefillParams {
 cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq, int half,
                                cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int d, int heads_per_cta, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, int cache_batch,
+                           cudaStream_t stream);
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd);
 int decode_key_tile();
 int prefill_key_tile();

@@ -1,72 +1,90 @@
 // prefill.cu -- causal GQA attention of a chunk of new tokens against the
-// per-sequence KV cache (cortiq-engine src/attention.rs, fn
-// qwen_attention_batch: query bi of a chunk sees keys 0 .. s0 + bi, i.e. all
-// history and the earlier keys of its own chunk; fn attention_head for the
-// softmax(q.k * scale) . V of each row; fn apply_gate for the sigmoid gate).
+// per-sequence KV cache, on the sm_100-family tensor cores (tcgen05 + TMEM +
+// TMA).  Semantics: cortiq-engine src/attention.rs, fn qwen_attention_batch
+// (query bi of a chunk sees keys 0 .. s0 + bi: all history and the earlier
+// keys of its own chunk), fn attention_head (softmax(q.k * scale) . V per row)
+// and fn apply_gate (sigmoid gate on the output).
 //
-// Flash-attention tiling: a CTA owns 64 query rows of one (sequence, query
-// head) and walks the key tiles of kv head h / (H / KV) that its rows can see,
-// with an online softmax in fp32 (log2 domain).  Key tiles wholly above the
-// diagonal are never loaded; only tiles that straddle it are masked.  When a
-// launch would leave SMs idle (short chunks), the keys are split across CTAs
-// and a combine pass merges the partial (max, sum, output) triples.
+// One CTA owns 128 query rows of one (sequence, query head) -- the 128 lanes of
+// tensor memory -- and walks the 128-key tiles of kv head h / (H / KV) that
+// those rows can see (tiles wholly above the diagonal are never loaded).
+// Warp roles:
+//   warp 0     TMA producer: Q tile once, then K and V tiles into a 2-stage
+//              ring (128-byte swizzled, as the MMA descriptors expect);
+//   warp 1     allocates tensor memory; one lane issues every tcgen05.mma:
+//              S_j = Q K_j^T (SS, both K-major) into one of three S buffers,
+//              then O += P_{j-1} V_{j-1} (TS: P read from tensor memory,
+//              V MN-major), committing each group to mbarriers;
+//   warps 4-7  softmax, one query row per thread (its TMEM lane): load S_j,
+//              mask, online max (log2 domain; the reference max is raised only
+//              when it grows by more than 2^8, and only then is the O row
+//              rescaled in tensor memory), exponentiate, write P_j as bf16 over
+//              the S buffer, and finally normalise, gate and store O.
+// The tensor core computes S_{j+1} while the softmax works on tile j, and
+// PV_{j-1} runs while the softmax prepares P_j.
+//
+// When a launch would leave most SMs idle (short chunks), keys are split
+// across CTAs and a combine pass merges the partial (max, sum, output) rows.
+// Every mbarrier wait is bounded; a timeout reports NA_ERR_DEVICE_TIMEOUT.
+#include <cuda.h>
+#include <mutex>
+
 #include "na_internal.cuh"
+#include "tc_primitives.cuh"
 
 namespace {
 
-constexpr int BM = 64;       // query rows per CTA
-constexpr int BN = 64;       // keys per tile
-constexpr int THREADS = 128; // 4 warps x 16 rows
+constexpr int BM = 128;      // query rows per CTA (tensor-memory lanes)
+constexpr int BN = 128;      // keys per tile
+constexpr int STAGES = 2;    // K/V shared-memory ring depth
+constexpr int NUM_S = 3;     // S/P buffers in tensor memory
+constexpr int THREADS = 256; // 8 warps: producer, MMA, two idle, four softmax
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL0 = 128;  // S buffer i at columns 128 (i + 1); O at column 0
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Element offset of 16-byte chunk `c` of row `r` in a swizzled [rows][D] tile.
 template <int D>
-__device__ __forceinline__ int swz(int r, int c)
+struct __align__(1024) TcSmem {
+    static constexpr int KB = D / 64;  // 64-wide column blocks of a row
+    bf16 q[KB][BM * 64];
+    bf16 k[STAGES][KB][BN * 64];
+    bf16 v[STAGES][KB][BN * 64];
+    uint64_t q_full;
+    uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+    uint64_t s_full[NUM_S], s_free[NUM_S], p_full[NUM_S];
+    uint64_t o_done, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int D>
+constexpr size_t tc_smem_bytes()
 {
-    return r * D + ((c ^ (r & 7)) << 3);
+    // at least ~116 KB so that a single CTA owns the SM (and its tensor memory)
+    return (sizeof(TcSmem<D>) + 1024) > (116u << 10) ? sizeof(TcSmem<D>) + 1024 : (116u << 10);
+}
+
+__device__ __forceinline__ bool aborted(const int *flag) { return *(volatile const int *)flag != 0; }
+
+__device__ __forceinline__ void set_abort(int *flag, int32_t *status)
+{
+    *(volatile int *)flag = 1;
+    na_report(status, NA_ERR_DEVICE_TIMEOUT);
 }
 
 template <int D>
-__global__ void __launch_bounds__(THREADS, 2) prefill_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(THREADS, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap map_q,
+                      const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v)
 {
-    constexpr int CH = D / 8;  // 16-byte chunks per row
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    bf16 *sQ = reinterpret_cast<bf16 *>(smem_raw);
-    bf16 *sK = sQ + BM * D;      // [2][BN][D]
-    bf16 *sV = sK + 2 * BN * D;  // [2][BN][D]
+    constexpr int KB = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    TcSmem<D> &sm = *reinterpret_cast<TcSmem<D> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int qt = blockIdx.x, h = blockIdx.y;
+    // ------------------------------------------------------------ the tile --
+    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
+    const int h = blockIdx.y;
     const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
     const int tok0 = __ldg(p.cu_seqlens + b);
     const int n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
@@ -93,194 +111,306 @@ __global__ void __launch_bounds__(THREADS, 2) prefill_kernel(const PrefillParams
     }
     if (k_begin >= k_end)
         return;
-
+    const int n_tiles = (k_end - k_begin + BN - 1) / BN;
     const int kvh = h / p.group;
-    const size_t cap = (size_t)p.capacity;
-    const bf16 *kbase = p.cache_k + ((size_t)b * p.KV + kvh) * cap * D;
-    const bf16 *vbase = p.cache_v + ((size_t)b * p.KV + kvh) * cap * D;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Q tile (rows past the chunk are zero-filled).
-    for (int c = tid; c < BM * CH; c += THREADS) {
-        const int r = c / CH, ch = c - r * CH;
-        const bool valid = r < rows;
-        const bf16 *src = p.q + ((size_t)(tok0 + r0 + (valid ? r : 0)) * p.H + h) * D + ch * 8;
-        cp_async16(sQ + swz<D>(r, ch), src, valid);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(&sm.k_full[s], 1);
+            mbar_init(&sm.v_full[s], 1);
+            mbar_init(&sm.k_empty[s], 1);
+            mbar_init(&sm.v_empty[s], 1);
+        }
+        for (int s = 0; s < NUM_S; s++) {
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.s_free[s], 1);
+            mbar_init(&sm.p_full[s], 4);
+        }
+        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        fence_barrier_init();
     }
-    auto load_kv = [&](int tile, int buf) {
-        const int j0 = tile * BN;
-        for (int c = tid; c < BN * CH; c += THREADS) {
-            const int r = c / CH, ch = c - r * CH;
-            const int j = j0 + r;
-            const bool valid = j < k_end;
-            const size_t off = (size_t)(valid ? j : 0) * D + ch * 8;
-            cp_async16(sK + buf * BN * D + swz<D>(r, ch), kbase + off, valid);
-            cp_async16(sV + buf * BN * D + swz<D>(r, ch), vbase + off, valid);
-        }
-    };
-    const int t_first = k_begin / BN, t_last = (k_end - 1) / BN;
-    load_kv(t_first, 0);
-    cp_async_commit();
+    if (warp == 1)
+        tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = sm.tmem_base;
 
-    const int g = lane >> 2, tq = lane & 3;
-    const int wrow = warp * 16;  // first row of this warp within the tile
-    const int pos0 = pos_lo + wrow + g, pos1 = pos0 + 8;
-
-    uint32_t qf[D / 16][4];
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; i++)
-        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int tile = t_first; tile <= t_last; tile++) {
-        const int buf = (tile - t_first) & 1;
-        if (tile < t_last) {
-            load_kv(tile + 1, buf ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        if (tile == t_first) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++) {
-                const int r = wrow + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4(qf[kk], sQ + swz<D>(r, kk * 2 + (lane >> 4)));
-            }
-        }
-        const bf16 *kt = sK + buf * BN * D;
-        const bf16 *vt = sV + buf * BN * D;
-
-        float s[BN / 8][4];
-#pragma unroll
-        for (int i = 0; i < BN / 8; i++)
-            s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk++) {
-#pragma unroll
-            for (int np = 0; np < BN / 16; np++) {
-                uint32_t bfr[4];
-                const int r = np * 16 + (lane & 7) + (lane >> 4) * 8;
-                ldsm_x4(bfr, kt + swz<D>(r, kk * 2 + ((lane >> 3) & 1)));
-                mma_bf16_16816(s[2 * np], qf[kk], bfr[0], bfr[1]);
-                mma_bf16_16816(s[2 * np + 1], qf[kk], bfr[2], bfr[3]);
-            }
-        }
-        const int j0 = tile * BN;
-        const bool need_mask = (j0 + BN - 1 > pos_lo) || (j0 + BN > k_end) || (j0 < k_begin);
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < BN / 8; nt++) {
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                float v0 = s[nt][e] * p.scale_log2, v1 = s[nt][2 + e] * p.scale_log2;
-                if (need_mask) {
-                    const int j = j0 + nt * 8 + 2 * tq + e;
-                    const bool kin = j >= k_begin && j < k_end;
-                    if (!kin || j > pos0)
-                        v0 = -INFINITY;
-                    if (!kin || j > pos1)
-                        v1 = -INFINITY;
+    if (warp == 0) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            tc::prefetch_tmap(&map_q);
+            tc::prefetch_tmap(&map_k);
+            tc::prefetch_tmap(&map_v);
+            const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
+            mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
+            for (int kb = 0; kb < KB; kb++)
+                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, tok0 + r0, &sm.q_full);
+            int issued = 0;
+            for (int j = 0; j < n_tiles; j++) {
+                const int st = j % STAGES;
+                const uint32_t par = ((j / STAGES) & 1) ^ 1;
+                if (!mbar_wait_bounded(&sm.k_empty[st], par) || aborted(&sm.abort_flag)) {
+                    set_abort(&sm.abort_flag, p.status);
+                    break;
                 }
-                s[nt][e] = v0;
-                s[nt][2 + e] = v1;
-                mx0 = fmaxf(mx0, v0);
-                mx1 = fmaxf(mx1, v1);
+                mbar_arrive_expect_tx(&sm.k_full[st], KB * BN * 128);
+                for (int kb = 0; kb < KB; kb++)
+                    tc::tma_load_2d(sm.k[st][kb], &map_k, kb * 64, row_base + j * BN, &sm.k_full[st]);
+                if (!mbar_wait_bounded(&sm.v_empty[st], par) || aborted(&sm.abort_flag)) {
+                    set_abort(&sm.abort_flag, p.status);
+                    mbar_wait_bounded(&sm.k_full[st], (j / STAGES) & 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.v_full[st], KB * BN * 128);
+                for (int kb = 0; kb < KB; kb++)
+                    tc::tma_load_2d(sm.v[st][kb], &map_v, kb * 64, row_base + j * BN, &sm.v_full[st]);
+                issued = j + 1;
+            }
+            // every copy issued lands before the CTA can exit
+            mbar_wait_bounded(&sm.q_full, 0);
+            for (int j = issued - 1; j >= 0 && j >= issued - STAGES; j--) {
+                mbar_wait_bounded(&sm.k_full[j % STAGES], (j / STAGES) & 1);
+                mbar_wait_bounded(&sm.v_full[j % STAGES], (j / STAGES) & 1);
             }
         }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);  // 0 when m was -inf
-        m0 = mn0;
-        m1 = mn1;
-        float rs0 = 0.f, rs1 = 0.f;
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issue --
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, D, false, true);
+            bool ok = mbar_wait_bounded(&sm.q_full, 0);
+            bool any = false;
+            for (int j = 0; ok && j <= n_tiles; j++) {
+                if (j < n_tiles) {
+                    const int st = j % STAGES, sb = j % NUM_S;
+                    ok = mbar_wait_bounded(&sm.k_full[st], (j / STAGES) & 1);
+                    if (ok && j >= NUM_S)
+                        ok = mbar_wait_bounded(&sm.s_free[sb], ((j / NUM_S) - 1) & 1);
+                    if (!ok || aborted(&sm.abort_flag))
+                        break;
+                    tc::fence_after_sync();
+                    const uint32_t s_t = tmem + S_COL0 * (sb + 1);
 #pragma unroll
-        for (int nt = 0; nt < BN / 8; nt++) {
-            s[nt][0] = exp2f(s[nt][0] - ref0);
-            s[nt][1] = exp2f(s[nt][1] - ref0);
-            s[nt][2] = exp2f(s[nt][2] - ref1);
-            s[nt][3] = exp2f(s[nt][3] - ref1);
-            rs0 += s[nt][0] + s[nt][1];
-            rs1 += s[nt][2] + s[nt][3];
-        }
-        l0 = l0 * a0 + rs0;
-        l1 = l1 * a1 + rs1;
+                    for (int k = 0; k < D / 16; k++) {
+                        const int kb = k >> 2, kk = k & 3;
+                        const uint64_t a = tc::desc_kmajor_sw128(smem_addr(sm.q[kb]) + kk * 32);
+                        const uint64_t bd = tc::desc_kmajor_sw128(smem_addr(sm.k[st][kb]) + kk * 32);
+                        tc::mma_ss(s_t, a, bd, idesc_s, k > 0);
+                    }
+                    tc::mma_commit(&sm.s_full[sb]);
+                    tc::mma_commit(&sm.k_empty[st]);
+                    any = true;
+                }
+                if (j >= 1) {
+                    const int jj = j - 1;
+                    const int st = jj % STAGES, sb = jj % NUM_S;
+                    ok = mbar_wait_bounded(&sm.p_full[sb], (jj / NUM_S) & 1);
+                    if (ok)
+                        ok = mbar_wait_bounded(&sm.v_full[st], (jj / STAGES) & 1);
+                    if (!ok || aborted(&sm.abort_flag))
+                        break;
+                    tc::fence_after_sync();
+                    const uint32_t p_t = tmem + S_COL0 * (sb + 1);
+                    const uint32_t vbase = smem_addr(sm.v[st][0]);
 #pragma unroll
-        for (int i = 0; i < D / 8; i++) {
-            o[i][0] *= a0;
-            o[i][1] *= a0;
-            o[i][2] *= a1;
-            o[i][3] *= a1;
-        }
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; kk++) {
-            uint32_t a[4];
-            a[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-            a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-            a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-            for (int dp = 0; dp < D / 16; dp++) {
-                uint32_t bfr[4];
-                const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4_t(bfr, vt + swz<D>(r, dp * 2 + (lane >> 4)));
-                mma_bf16_16816(o[2 * dp], a, bfr[0], bfr[1]);
-                mma_bf16_16816(o[2 * dp + 1], a, bfr[2], bfr[3]);
+                    for (int k = 0; k < BN / 16; k++) {
+                        const uint64_t bd = tc::desc_mnmajor_sw128(vbase + k * 16 * 128, BN * 128);
+                        tc::mma_ts(tmem, p_t + k * 8, bd, idesc_o, jj > 0 || k > 0);
+                    }
+                    tc::mma_commit(&sm.s_free[sb]);
+                    tc::mma_commit(&sm.v_empty[st]);
+                    tc::mma_commit(&sm.o_done);
+                }
+            }
+            if (!ok)
+                set_abort(&sm.abort_flag, p.status);
+            if (any) {  // all issued MMAs complete before tensor memory is released
+                tc::mma_commit(&sm.drain);
+                mbar_wait_bounded(&sm.drain, 0);
             }
         }
-        __syncthreads();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- softmax --
+        const int r = (warp - 4) * 32 + lane;  // query row == TMEM lane
+        const int row_pos = pos_lo + r;
+        const uint32_t lane_off = tc::tmem_lane_base(warp);
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; j++) {
+            const int sb = j % NUM_S;
+            const int j0 = k_begin + j * BN;
+            const uint32_t s_t = tmem + S_COL0 * (sb + 1) + lane_off;
+            if (!mbar_wait_bounded(&sm.s_full[sb], (j / NUM_S) & 1) || aborted(&sm.abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                tc::tmem_ld32(s_t + c * 32, sr[c]);
+            tc::tmem_wait_ld();
+
+            const bool need_mask = (j0 + BN - 1 > pos_lo) || (j0 + BN > k_end);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    float s = __uint_as_float(sr[c][i]);
+                    if (need_mask) {
+                        const int key = j0 + c * 32 + i;
+                        if (key > row_pos || key >= k_end)
+                            s = -INFINITY;
+                    }
+                    sr[c][i] = __float_as_uint(s);
+                    mx = fmaxf(mx, s);
+                }
+            const float mxs = mx * sl2;
+            float alpha = 1.f;
+            bool corr = false;
+            if (mxs > m_ref + 8.0f) {
+                alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mxs);
+                corr = (m_ref != -INFINITY);
+                m_ref = mxs;
+            }
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const float p0 = exp2f(fmaf(__uint_as_float(sr[c][2 * i]), sl2, neg_m));
+                    const float p1 = exp2f(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, neg_m));
+                    rs += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tc::tmem_st16(s_t + c * 16, pk);
+            }
+            tc::tmem_wait_st();
+
+            if (j0 + BN > k_end) {
+                // Key rows past the valid range hold whatever the cache has there;
+                // zero them in shared memory so P * V sees no non-finite values.
+                const int st = j % STAGES;
+                if (!mbar_wait_bounded(&sm.v_full[st], (j / STAGES) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (r >= k_end - j0) {
+#pragma unroll
+                    for (int kb = 0; kb < KB; kb++) {
+                        uint4 *row = reinterpret_cast<uint4 *>(sm.v[st][kb] + r * 64);
+#pragma unroll
+                        for (int c = 0; c < 8; c++)
+                            row[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                tc::fence_proxy_async_smem();
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, corr)) {
+                // rescale this warp's O rows once PV_{j-1} has landed
+                if (!mbar_wait_bounded(&sm.o_done, (j - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const float a = corr ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_off + c * 32, o);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                    tc::tmem_st32(tmem + lane_off + c * 32, o);
+                }
+                tc::tmem_wait_st();
+            }
+            l = l * alpha + rs;
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.p_full[sb]);
+        }
+        if (!ok) {
+            if (lane == 0)
+                set_abort(&sm.abort_flag, p.status);
+        } else if (mbar_wait_bounded(&sm.o_done, (n_tiles - 1) & 1)) {
+            // ---------------------------------------------------- epilogue --
+            tc::fence_after_sync();
+            const size_t t = (size_t)(tok0 + r0 + r);
+            const bool valid = r < rows;
+            if (p.num_splits == 1) {
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+                bf16 *dst = p.out + (t * p.H + h) * D;
+                const bool gated = (p.flags & NA_OUT_GATE) && p.gate;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_off + c * 32, o);
+                    tc::tmem_wait_ld();
+                    if (!valid)
+                        continue;
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        f[i] = __uint_as_float(o[i]) * inv;
+                    if (gated) {
+                        const uint4 *g4 = reinterpret_cast<const uint4 *>(p.gate + (t * p.H + h) * D + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            float g[8];
+                            bf16x8_to_f32(__ldg(g4 + q), g);
+#pragma unroll
+                            for (int e = 0; e < 8; e++)
+                                f[q * 8 + e] *= 1.0f / (1.0f + __expf(-g[e]));
+                        }
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        d4[q] = f32_to_bf16x8(f + q * 8);
+                }
+            } else {
+                const size_t row = (t * p.H + h) * p.num_splits + split;
+                float *dst = p.part_o + row * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_off + c * 32, o);
+                    tc::tmem_wait_ld();
+                    if (!valid)
+                        continue;
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; q++)
+                        d4[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                            __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+                }
+                if (valid) {
+                    p.part_ml[row * 2] = m_ref;
+                    p.part_ml[row * 2 + 1] = l;
+                }
+            }
+        } else if (lane == 0) {
+            set_abort(&sm.abort_flag, p.status);
+        }
     }
 
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    const int rr0 = wrow + g, rr1 = rr0 + 8;  // rows within the tile
-#pragma unroll
-    for (int half = 0; half < 2; half++) {
-        const int rr = half ? rr1 : rr0;
-        if (rr >= rows)
-            continue;
-        const size_t t = (size_t)(tok0 + r0 + rr);
-        const float l = half ? l1 : l0;
-        const float m = half ? m1 : m0;
-        if (p.num_splits == 1) {
-            const float inv = 1.0f / l;
-            bf16 *dst = p.out + (t * p.H + h) * D;
-            const bf16 *gt = ((p.flags & NA_OUT_GATE) && p.gate) ? p.gate + (t * p.H + h) * D : nullptr;
-#pragma unroll
-            for (int nt = 0; nt < D / 8; nt++) {
-                const int col = nt * 8 + 2 * tq;
-                float x0 = o[nt][2 * half] * inv, x1 = o[nt][2 * half + 1] * inv;
-                if (gt) {
-                    const __nv_bfloat162 gg = *reinterpret_cast<const __nv_bfloat162 *>(gt + col);
-                    x0 *= 1.0f / (1.0f + __expf(-__bfloat162float(gg.x)));
-                    x1 *= 1.0f / (1.0f + __expf(-__bfloat162float(gg.y)));
-                }
-                *reinterpret_cast<uint32_t *>(dst + col) = pack_bf16x2(x0, x1);
-            }
-        } else {
-            const size_t row = (t * p.H + h) * p.num_splits + split;
-            float *dst = p.part_o + row * D;
-#pragma unroll
-            for (int nt = 0; nt < D / 8; nt++) {
-                const int col = nt * 8 + 2 * tq;
-                *reinterpret_cast<float2 *>(dst + col) =
-                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-            }
-            if (tq == 0) {
-                p.part_ml[row * 2] = m;
-                p.part_ml[row * 2 + 1] = l;
-            }
-        }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -302,7 +432,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
             hi = mid - 1;
     }
     const int pos = __ldg(p.cache_lens + lo) + (t - __ldg(p.cu_seqlens + lo));
-    if (pos < 0 || pos >= p.capacity)
+    if (pos < 0 || pos >= p.capacity || pos >= p.max_total_len)
         return;  // reported by the split pass
     const int ns = min(p.num_splits, pos / p.split_len + 1);
     const float *ml = p.part_ml + (size_t)row * p.num_splits * 2;
@@ -310,42 +440,107 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     for (int s = 0; s < ns; s++)
         M = fmaxf(M, ml[2 * s]);
     float L = 0.f;
-    for (int s = 0; s < ns; s++)
+    float w[16];
+    for (int s = 0; s < ns && s < 16; s++) {
+        w[s] = exp2f(ml[2 * s] - M);
+        L += ml[2 * s + 1] * w[s];
+    }
+    for (int s = 16; s < ns; s++)
         L += ml[2 * s + 1] * exp2f(ml[2 * s] - M);
     const float inv = 1.0f / L;
     const float *po = p.part_o + (size_t)row * p.num_splits * D;
     bf16 *dst = p.out + (size_t)row * D;
     const bf16 *gt = ((p.flags & NA_OUT_GATE) && p.gate) ? p.gate + (size_t)row * D : nullptr;
-    for (int e = lane; e < D; e += 32) {
-        float o = 0.f;
-        for (int s = 0; s < ns; s++)
-            o += po[(size_t)s * D + e] * exp2f(ml[2 * s] - M);
-        o *= inv;
-        if (gt)
-            o *= 1.0f / (1.0f + __expf(-__bfloat162float(gt[e])));
-        dst[e] = __float2bfloat16_rn(o);
+    for (int e = lane * 2; e < D; e += 64) {
+        float o0 = 0.f, o1 = 0.f;
+        for (int s = 0; s < ns; s++) {
+            const float ws = s < 16 ? w[s] : exp2f(ml[2 * s] - M);
+            const float2 v = *reinterpret_cast<const float2 *>(po + (size_t)s * D + e);
+            o0 = fmaf(v.x, ws, o0);
+            o1 = fmaf(v.y, ws, o1);
+        }
+        o0 *= inv;
+        o1 *= inv;
+        if (gt) {
+            const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162 *>(gt + e);
+            o0 *= 1.0f / (1.0f + __expf(-__bfloat162float(g.x)));
+            o1 *= 1.0f / (1.0f + __expf(-__bfloat162float(g.y)));
+        }
+        *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(o0, o1);
     }
 }
 
-template <int D>
-cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, cudaStream_t stream)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
 {
-    const size_t smem = (size_t)(BM + 4 * BN) * D * sizeof(bf16);
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 64-element (128-byte) inner boxes and 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides_bytes, const cuuint32_t *box)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+              dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache_batch,
+                             cudaStream_t stream)
+{
+    CUtensorMap mq, mk, mv;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)total_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.H * D * 2};
+        const cuuint32_t box[3] = {64, 1, BM};
+        if (!make_map(&mq, p.q, 3, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t rows = (cuuint64_t)cache_batch * p.KV * p.capacity;
+        const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        const cuuint32_t box[2] = {64, BN};
+        if (!make_map(&mk, p.cache_k, 2, dims, strides, box) ||
+            !make_map(&mv, p.cache_v, 2, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    const size_t smem = tc_smem_bytes<D>();
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
     dim3 grid(p.q_tiles, p.H, p.batch * p.num_splits);
-    prefill_kernel<D><<<grid, THREADS, smem, stream>>>(p);
+    prefill_tc_kernel<D><<<grid, THREADS, smem, stream>>>(p, mq, mk, mv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1)
         return e;
-    const int rows = total_tokens * p.H;
-    prefill_combine_kernel<D><<<(rows + 7) / 8, 256, 0, stream>>>(p, total_tokens);
+    const int nrows = total_tokens * p.H;
+    prefill_combine_kernel<D><<<(nrows + 7) / 8, 256, 0, stream>>>(p, total_tokens);
     return cudaGetLastError();
 }
 
@@ -354,9 +549,10 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, cudaStrea
 int prefill_key_tile() { return BN; }
 int prefill_q_tile() { return BM; }
 
-cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, cudaStream_t stream)
+cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, int cache_batch,
+                           cudaStream_t stream)
 {
     if (d == 128)
-        return launch_prefill_t<128>(p, total_tokens, stream);
-    return launch_prefill_t<64>(p, total_tokens, stream);
+        return launch_prefill_t<128>(p, total_tokens, cache_batch, stream);
+    return launch_prefill_t<64>(p, total_tokens, cache_batch, stream);
 }
