@@ -13,13 +13,15 @@
 // tensor cores: per key the group does 2 * HPC * d flops over 4 d bytes, far
 // below the SIMT rate, so the pass is bound by HBM bandwidth.
 //
-// Consumer lane layout: a warp takes 4 keys per step (key group kg = lane / 8);
-// the 8 lanes of a key group split head_dim into 8 slices of d/8.  Each lane
-// forms HPC partial dot products, and a 3-level butterfly leaves the full score
-// of (key kg, head lane%8 / (8/HPC)) in that lane.  The running maximum is only
-// raised when a tile's maximum exceeds it by more than 2^8 (factor 256), so
-// the accumulator rescale runs a handful of times per split instead of per tile;
-// scores are carried in the log2 domain (q pre-scaled by scale * log2 e).
+// Consumer lane layout: a warp takes 2 keys per step (key group kg = lane / 16);
+// the 16 lanes of a key group split head_dim into slices of d/16 elements.
+// Each lane forms HPC partial dot products with packed fp32x2 FMAs, and a
+// 4-level butterfly leaves the full score of (key kg, head (lane%16) / (16/HPC))
+// in that lane.  The running maximum is only raised when a tile's maximum
+// exceeds it by more than 2^8 (factor 256), so the accumulator rescale runs a
+// handful of times per split instead of per tile; scores are carried in the
+// log2 domain (q pre-scaled by scale * log2 e).  Two CTAs share an SM (about
+// 112 KB of shared memory and <= 112 registers per thread each).
 //
 // Raw log2-domain scores are written to the probability buffer; the combine
 // pass turns them into probabilities once the global maximum and sum are known,
@@ -29,9 +31,11 @@
 namespace {
 
 constexpr int DEC_TILE = 64;
-constexpr int DEC_STAGES = 4;
+constexpr int DEC_STAGES = 3;
 constexpr int DEC_CWARPS = 8;
 constexpr int DEC_THREADS = (DEC_CWARPS + 1) * 32;
+constexpr int LPK = 16;                    // lanes per key
+constexpr int KPS = 32 / LPK;              // keys per warp step
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D, int HPC>
@@ -63,19 +67,41 @@ __device__ __forceinline__ Unit unit_of(int u, const DecodeParams &p)
 }
 
 // Key range [s0, s1) of a unit; empty when s0 >= s1.  Lengths past the cache
-// capacity or the workspace split count are reported and skipped.
+// capacity or the host bound are skipped here and reported by the combine pass.
 __device__ __forceinline__ void unit_keys(const Unit &w, const DecodeParams &p, int &s0, int &s1)
 {
     const int n = __ldg(p.kv_lens + w.b);
     s0 = w.split * p.split_len;
     s1 = min(n, s0 + p.split_len);
-    if (n < 0 || n > p.capacity || n > p.max_kv_len) {
-        s1 = s0;  // invalid length: the combine pass reports it
+    if (n < 0 || n > p.capacity || n > p.max_kv_len)
+        s1 = s0;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// N 32-bit words (2N bf16) from a 16-byte (N = 4) or 8-byte (N = 2) aligned address.
+template <int N>
+__device__ __forceinline__ void load_words(const bf16 *src, uint32_t (&w)[N])
+{
+    if constexpr (N == 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        w[0] = u.x;
+        w[1] = u.y;
+        w[2] = u.z;
+        w[3] = u.w;
+    } else {
+        static_assert(N == 2, "2 or 4 words");
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        w[0] = u.x;
+        w[1] = u.y;
     }
 }
 
 template <int D, int HPC>
-__global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const DecodeParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     DecSmem<D, HPC> &sm = *reinterpret_cast<DecSmem<D, HPC> *>(smem_raw);
@@ -125,7 +151,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const Deco
             }
         }
         // Let every copy this lane issued land before the CTA can exit.
-        for (int s = 0; s < DEC_STAGES && it > 0; s++) {
+        for (int s = 0; s < DEC_STAGES; s++) {
             if ((int)it - 1 - s < 0)
                 break;
             const uint32_t last = it - 1 - s;
@@ -135,10 +161,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const Deco
     }
 
     // ------------------------------------------------------------ consumers --
-    constexpr int EPL = D / 8;   // head_dim elements per lane
-    constexpr int R = 8 / HPC;   // lanes holding the same (key, head) score
-    const int kg = lane >> 3, sub = lane & 7;
-    const int hsel = sub / R;    // head whose score this lane ends up holding
+    constexpr int EPL = D / LPK;   // head_dim elements per lane
+    constexpr int R = LPK / HPC;   // lanes holding the same (key, head) score
+    constexpr int KPW = DEC_TILE / DEC_CWARPS;  // keys per warp per tile
+    constexpr int STEPS = KPW / KPS;
+    const int kg = lane / LPK, sub = lane % LPK;
+    const int hsel = sub / R;      // head whose score this lane ends up holding
     const unsigned FULL = 0xffffffffu;
     uint32_t it = 0;
     // A warp whose wait timed out keeps walking the units so that every warp
@@ -155,28 +183,25 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const Deco
             aborted = true;
         const int head0 = w.kvh * p.group + w.hc * HPC;
 
-        float q[HPC][EPL];
+        float2 q[HPC][EPL / 2];
 #pragma unroll
         for (int h = 0; h < HPC; h++) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q + ((size_t)w.b * p.H + head0 + h) * D + sub * EPL);
+            uint32_t wd[EPL / 2];
+            load_words<EPL / 2>(p.q + ((size_t)w.b * p.H + head0 + h) * D + sub * EPL, wd);
 #pragma unroll
-            for (int c = 0; c < EPL / 8; c++) {
-                float f[8];
-                bf16x8_to_f32(__ldg(src + c), f);
-#pragma unroll
-                for (int e = 0; e < 8; e++)
-                    q[h][c * 8 + e] = f[e] * p.scale_log2;
+            for (int e = 0; e < EPL / 2; e++) {
+                const float2 f = bf16x2_to_f2(wd[e]);
+                q[h][e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
             }
         }
-        float acc[HPC][EPL];
+        float2 acc[HPC][EPL / 2];
         float m_ref[HPC];
 #pragma unroll
         for (int h = 0; h < HPC; h++) {
             m_ref[h] = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < EPL; e++)
-                acc[h][e] = 0.f;
+            for (int e = 0; e < EPL / 2; e++)
+                acc[h][e] = make_float2(0.f, 0.f);
         }
         float l_lane = 0.f;
         float *probs_row = p.probs ? p.probs + ((size_t)w.b * p.H + head0 + hsel) * p.probs_stride
@@ -194,62 +219,62 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const Deco
             }
             const bf16 *kt = sm.k[stage];
             const bf16 *vt = sm.v[stage];
-            constexpr int KPW = DEC_TILE / DEC_CWARPS;  // keys per warp per tile
-            constexpr int STEPS = KPW / 4;
+            const bool full_tile = j0 + DEC_TILE <= s1;
             float s[STEPS];
 #pragma unroll
             for (int st = 0; st < STEPS; st++) {
-                const int kl = warp * KPW + st * 4 + kg;  // key within the tile
-                const uint4 *krow = reinterpret_cast<const uint4 *>(kt + kl * D + sub * EPL);
+                const int kl = warp * KPW + st * KPS + kg;  // key within the tile
+                float2 part2[HPC];
+#pragma unroll
+                for (int h = 0; h < HPC; h++)
+                    part2[h] = make_float2(0.f, 0.f);
+                uint32_t wd[EPL / 2];
+                load_words<EPL / 2>(kt + kl * D + sub * EPL, wd);
+#pragma unroll
+                for (int e = 0; e < EPL / 2; e++) {
+                    const float2 kf = bf16x2_to_f2(wd[e]);
+#pragma unroll
+                    for (int h = 0; h < HPC; h++)
+                        part2[h] = __ffma2_rn(q[h][e], kf, part2[h]);
+                }
                 float part[HPC];
 #pragma unroll
                 for (int h = 0; h < HPC; h++)
-                    part[h] = 0.f;
-#pragma unroll
-                for (int c = 0; c < EPL / 8; c++) {
-                    float f[8];
-                    bf16x8_to_f32(krow[c], f);
-#pragma unroll
-                    for (int e = 0; e < 8; e++)
-#pragma unroll
-                        for (int h = 0; h < HPC; h++)
-                            part[h] = fmaf(q[h][c * 8 + e], f[e], part[h]);
-                }
-                // Butterfly over the 8 lanes of the key group: halve the head
+                    part[h] = part2[h].x + part2[h].y;
+                // Butterfly over the LPK lanes of the key group: halve the head
                 // set at each level while it has more than one head.
-                float val;
-                if constexpr (HPC == 4) {
-                    const bool up = (sub & 4) != 0;
-                    float a0 = up ? part[2] : part[0], a1 = up ? part[3] : part[1];
-                    const float b0 = up ? part[0] : part[2], b1 = up ? part[1] : part[3];
-                    a0 += __shfl_xor_sync(FULL, b0, 4);
-                    a1 += __shfl_xor_sync(FULL, b1, 4);
-                    const bool up2 = (sub & 2) != 0;
-                    val = (up2 ? a1 : a0) + __shfl_xor_sync(FULL, up2 ? a0 : a1, 2);
-                    val += __shfl_xor_sync(FULL, val, 1);
-                } else if constexpr (HPC == 2) {
-                    const bool up = (sub & 4) != 0;
-                    val = (up ? part[1] : part[0]) + __shfl_xor_sync(FULL, up ? part[0] : part[1], 4);
-                    val += __shfl_xor_sync(FULL, val, 2);
-                    val += __shfl_xor_sync(FULL, val, 1);
-                } else {
-                    val = part[0];
-                    val += __shfl_xor_sync(FULL, val, 4);
-                    val += __shfl_xor_sync(FULL, val, 2);
-                    val += __shfl_xor_sync(FULL, val, 1);
+                int cnt = HPC;
+#pragma unroll
+                for (int m = LPK / 2; m >= 1; m >>= 1) {
+                    if (cnt > 1) {
+                        const bool up = (sub & m) != 0;
+                        const int half = cnt / 2;
+#pragma unroll
+                        for (int i = 0; i < HPC / 2; i++) {
+                            if (i < half) {
+                                const float keep = up ? part[half + i] : part[i];
+                                const float send = up ? part[i] : part[half + i];
+                                part[i] = keep + __shfl_xor_sync(FULL, send, m);
+                            }
+                        }
+                        cnt = half;
+                    } else {
+                        part[0] += __shfl_xor_sync(FULL, part[0], m);
+                    }
                 }
                 const int j = j0 + kl;
-                s[st] = (j < s1) ? val : -INFINITY;
-                if (probs_row && j < s1 && (sub % R) == 0)
-                    probs_row[j] = val;
+                s[st] = (full_tile || j < s1) ? part[0] : -INFINITY;
+                if (probs_row && (full_tile || j < s1) && (sub % R) == 0)
+                    probs_row[j] = part[0];
             }
             // Tile maximum per head, then (rarely) raise the reference maximum.
             float tmax = s[0];
 #pragma unroll
             for (int st = 1; st < STEPS; st++)
                 tmax = fmaxf(tmax, s[st]);
-            tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 8));
-            tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 16));
+#pragma unroll
+            for (int m = LPK; m < 32; m <<= 1)
+                tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, m));
             float hmax[HPC];
             bool raise = false;
 #pragma unroll
@@ -263,9 +288,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const Deco
                     const float m_new = fmaxf(m_ref[h], hmax[h]);
                     const float alpha = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - m_new);
                     m_ref[h] = m_new;
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int e = 0; e < EPL; e++)
-                        acc[h][e] *= alpha;
+                    for (int e = 0; e < EPL / 2; e++)
+                        acc[h][e] = __fmul2_rn(acc[h][e], a2);
                     if (h == hsel)
                         l_lane *= alpha;
                 }
@@ -279,46 +305,49 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_split_kernel(const Deco
             for (int st = 0; st < STEPS; st++) {
                 const float pr = (s[st] == -INFINITY) ? 0.f : exp2f(s[st] - m_mine);
                 l_lane += pr;
-                const int kl = warp * KPW + st * 4 + kg;
-                const bool valid = (j0 + kl) < s1;
-                float pv[HPC];
+                const int kl = warp * KPW + st * KPS + kg;
+                const bool valid = full_tile || (j0 + kl) < s1;
+                float2 pv[HPC];
 #pragma unroll
-                for (int h = 0; h < HPC; h++)
-                    pv[h] = __shfl_sync(FULL, pr, kg * 8 + h * R);
-                const uint4 *vrow = reinterpret_cast<const uint4 *>(vt + kl * D + sub * EPL);
+                for (int h = 0; h < HPC; h++) {
+                    const float x = __shfl_sync(FULL, pr, kg * LPK + h * R);
+                    pv[h] = make_float2(x, x);
+                }
+                uint32_t wd[EPL / 2];
+                load_words<EPL / 2>(vt + kl * D + sub * EPL, wd);
 #pragma unroll
-                for (int c = 0; c < EPL / 8; c++) {
-                    float f[8];
-                    bf16x8_to_f32(vrow[c], f);
+                for (int e = 0; e < EPL / 2; e++) {
+                    float2 vf = bf16x2_to_f2(wd[e]);
+                    if (!valid)  // stale shared memory past the last key
+                        vf = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        const float ve = valid ? f[e] : 0.f;
-#pragma unroll
-                        for (int h = 0; h < HPC; h++)
-                            acc[h][c * 8 + e] = fmaf(pv[h], ve, acc[h][c * 8 + e]);
-                    }
+                    for (int h = 0; h < HPC; h++)
+                        acc[h][e] = __ffma2_rn(pv[h], vf, acc[h][e]);
                 }
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.empty[stage]);
         }
-        // Merge the four key groups of the warp, then the warps of the CTA.
+
+        // Merge the key groups of the warp, then the warps of the CTA.
 #pragma unroll
-        for (int h = 0; h < HPC; h++)
+        for (int m = LPK; m < 32; m <<= 1) {
 #pragma unroll
-            for (int e = 0; e < EPL; e++) {
-                acc[h][e] += __shfl_xor_sync(FULL, acc[h][e], 8);
-                acc[h][e] += __shfl_xor_sync(FULL, acc[h][e], 16);
-            }
-        l_lane += __shfl_xor_sync(FULL, l_lane, 8);
-        l_lane += __shfl_xor_sync(FULL, l_lane, 16);
+            for (int h = 0; h < HPC; h++)
+#pragma unroll
+                for (int e = 0; e < EPL / 2; e++) {
+                    acc[h][e].x += __shfl_xor_sync(FULL, acc[h][e].x, m);
+                    acc[h][e].y += __shfl_xor_sync(FULL, acc[h][e].y, m);
+                }
+            l_lane += __shfl_xor_sync(FULL, l_lane, m);
+        }
         if (kg == 0) {
 #pragma unroll
             for (int h = 0; h < HPC; h++)
 #pragma unroll
-                for (int e = 0; e < EPL; e++)
-                    sm.merge_o[warp][h][sub * EPL + e] = acc[h][e];
+                for (int e = 0; e < EPL / 2; e++)
+                    *reinterpret_cast<float2 *>(&sm.merge_o[warp][h][sub * EPL + 2 * e]) = acc[h][e];
             if ((sub % R) == 0) {
                 float m_mine = m_ref[0];
 #pragma unroll
@@ -431,6 +460,9 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
         cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, HPC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_split_kernel<D, HPC>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess)
             return e;
         configured = true;
@@ -438,7 +470,7 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = p.total_units < sms ? p.total_units : sms;
+    const int grid = p.total_units < 2 * sms ? p.total_units : 2 * sms;  // two CTAs per SM
     if (grid > 0)
         decode_split_kernel<D, HPC><<<grid, DEC_THREADS, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();

@@ -118,7 +118,8 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     PrefillPlan pl{};
     const int bm = prefill_q_tile(), bn = prefill_key_tile();
     pl.q_tiles = (max_new_len + bm - 1) / bm;
-    const long long est = (long long)batch * pl.q_tiles * c->num_heads;
+    const int group = c->num_heads / c->num_kv_heads;
+    const long long est = (long long)batch * pl.q_tiles * c->num_kv_heads * ((group + 1) / 2);
     const long long target = 2ll * sm_count();
     int splits = 1;
     if (est < target && max_total_len > 2 * bn) {
