@@ -109,9 +109,11 @@ struct PrefillPlan {
     size_t ws_bytes;
 };
 
-// Split the keys across CTAs only when the (query tile, head, sequence) grid
-// would leave most SMs idle (one CTA owns an SM); the split count targets about
-// two CTAs per SM, each split covering at least two key tiles.
+// Split the keys across CTAs only when the (query tile, head pair, sequence)
+// grid would leave most SMs idle (one CTA owns an SM); the split count targets
+// about one CTA per SM, each split covering at least four key tiles (fewer,
+// longer splits measured faster than more, shorter ones: less partial traffic
+// for the combine pass).
 PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int max_new_len,
                          int max_total_len)
 {
@@ -120,11 +122,11 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     pl.q_tiles = (max_new_len + bm - 1) / bm;
     const int group = c->num_heads / c->num_kv_heads;
     const long long est = (long long)batch * pl.q_tiles * c->num_kv_heads * ((group + 1) / 2);
-    const long long target = 2ll * sm_count();
+    const long long target = sm_count();
     int splits = 1;
-    if (est < target && max_total_len > 2 * bn) {
+    if (est < target && max_total_len > 4 * bn) {
         splits = (int)((target + est - 1) / est);
-        const int max_by_len = (max_total_len + 2 * bn - 1) / (2 * bn);
+        const int max_by_len = (max_total_len + 4 * bn - 1) / (4 * bn);
         splits = splits < max_by_len ? splits : max_by_len;
         if (splits < 1)
             splits = 1;
