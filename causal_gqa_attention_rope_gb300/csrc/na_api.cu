@@ -109,7 +109,7 @@ struct PrefillPlan {
     size_t ws_bytes;
 };
 
-// Split the keys across CTAs only when the (query tile, head pair, sequence)
+// Split the keys across CTAs only when the (query tile, head, sequence)
 // grid would leave most SMs idle (one CTA owns an SM); the split count targets
 // about one CTA per SM, each split covering at least four key tiles (fewer,
 // longer splits measured faster than more, shorter ones: less partial traffic
@@ -120,8 +120,7 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     PrefillPlan pl{};
     const int bm = prefill_q_tile(), bn = prefill_key_tile();
     pl.q_tiles = (max_new_len + bm - 1) / bm;
-    const int group = c->num_heads / c->num_kv_heads;
-    const long long est = (long long)batch * pl.q_tiles * c->num_kv_heads * ((group + 1) / 2);
+    const long long est = (long long)batch * pl.q_tiles * c->num_heads;
     const long long target = sm_count();
     int splits = 1;
     if (est < target && max_total_len > 4 * bn) {

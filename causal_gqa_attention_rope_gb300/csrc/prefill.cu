@@ -5,27 +5,27 @@
 // keys of its own chunk), fn attention_head (softmax(q.k * scale) . V per row)
 // and fn apply_gate (sigmoid gate on the output).
 //
-// One CTA owns 128 query tokens of one sequence for two query heads of the
-// same GQA group (tiles A and B: same positions, same keys, same causal mask;
-// an odd group leaves the last CTA of the group with tile A only).  Each tile
-// fills the 128 lanes of tensor memory; both read the same 128-key tiles of kv
-// head h / (H / KV), so every K and V tile in shared memory feeds two MMAs.
-// Key tiles wholly above the diagonal are never loaded.
-// Warp roles (10 warps):
-//   warp 0     TMA producer: the two Q tiles once, then K and V tiles into a
-//              2-stage ring (128-byte swizzled, as the MMA descriptors expect);
-//   warp 1     allocates tensor memory; one lane issues every tcgen05.mma, per
-//              key tile j: S_A = Q_A K_j^T, S_B = Q_B K_j^T (SS, K-major), then
-//              O_A += P_A V_j, O_B += P_B V_j (TS: P read from tensor memory,
-//              V MN-major), committing each group to mbarriers;
-//   warps 2-5  softmax of tile A, one query row per thread (its TMEM lane);
-//   warps 6-9  softmax of tile B.
-// Softmax: load S, mask, online max in the log2 domain (the reference max is
-// raised only when it grows by more than 2^8, and only then is the O row
-// rescaled in tensor memory), exponentiate, write P as bf16 over S, and finally
-// normalise, gate and store O.  While one warpgroup exponentiates, the tensor
-// core runs the other tile's MMAs.  A quarter of the exponentials run on the
-// FMA pipe (exp2_poly) so the MUFU unit is not the bottleneck.
+// One CTA owns 128 query rows of one (sequence, query head) -- the 128 lanes
+// of tensor memory -- and walks the 128-key tiles of kv head h / (H / KV) that
+// those rows can see (tiles wholly above the diagonal are never loaded).
+// Warp roles (8 warps):
+//   warp 0     TMA producer: the Q tile once, then K and V tiles into a
+//              3-stage ring (128-byte swizzled, as the MMA descriptors expect);
+//   warp 1     allocates tensor memory; one lane issues S_j = Q K_j^T (SS, both
+//              K-major) into one of three S buffers in tensor memory;
+//   warp 2     one lane issues O += P_j V_j (TS: P read from tensor memory over
+//              S_j, V MN-major).  Two issuing threads, because one thread cannot
+//              keep the tensor core busy with M = N = 128 instructions (each
+//              takes ~116 SM cycles to issue, measured on GB300, against ~64
+//              cycles of math);
+//   warps 4-7  softmax, one query row per thread (its TMEM lane): load S_j,
+//              mask, online max in the log2 domain (the reference max is raised
+//              only when it grows by more than 2^8, and only then is the O row
+//              rescaled in tensor memory), exponentiate (a quarter on the FMA
+//              pipe, exp2_poly, the rest on MUFU), write P_j as bf16 over S_j,
+//              and finally normalise, gate and store O.
+// With three S buffers the tensor core computes S_{j+1} and S_{j+2} while the
+// softmax works on tile j, and PV_j runs while it prepares P_{j+1}.
 //
 #include <cuda.h>
 #include <mutex>
@@ -35,27 +35,25 @@
 
 namespace {
 
-constexpr int BM = 128;      // query rows per tile (tensor-memory lanes)
+constexpr int BM = 128;      // query rows per CTA (tensor-memory lanes)
 constexpr int BN = 128;      // keys per tile
-constexpr int STAGES = 2;    // K/V shared-memory ring depth
-constexpr int THREADS = 320; // 10 warps: producer, MMA, 2 x 4 softmax
+constexpr int STAGES = 3;    // K/V shared-memory ring depth
+constexpr int NUM_S = 3;     // S/P buffers in tensor memory
+constexpr int THREADS = 256; // 8 warps: producer, S issuer, PV issuer, idle, 4 softmax
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int POLY_CHUNKS = 1;  // 32-column chunks of each S row exponentiated on the FMA pipe
-
-// Tensor-memory columns: O_A [0,128), O_B [128,256), S_A [256,384), S_B [384,512).
-__device__ __forceinline__ uint32_t o_col(int t) { return (uint32_t)t * 128u; }
-__device__ __forceinline__ uint32_t s_col(int t) { return 256u + (uint32_t)t * 128u; }
+constexpr uint32_t S_COL0 = 128;  // S buffer i at columns 128 (i + 1); O at column 0
+constexpr int POLY_CHUNKS = 1;    // 32-column chunks of each S row exponentiated on the FMA pipe
 
 template <int D>
 struct __align__(1024) TcSmem {
     static constexpr int KB = D / 64;  // 64-wide column blocks of a row
-    bf16 q[2][KB][BM * 64];
+    bf16 q[KB][BM * 64];
     bf16 k[STAGES][KB][BN * 64];
     bf16 v[STAGES][KB][BN * 64];
     uint64_t q_full;
     uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-    uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
-    uint64_t drain;
+    uint64_t s_full[NUM_S], s_free[NUM_S], p_full[NUM_S];
+    uint64_t o_done, drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -118,16 +116,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     // ------------------------------------------------------------ the tile --
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const int pairs = (p.group + 1) / 2;
-    const int kvh = blockIdx.y / pairs, pair = blockIdx.y - kvh * pairs;
-    const int head0 = kvh * p.group + 2 * pair;  // tile t is query head head0 + t
-    const int ntile = (2 * pair + 1 < p.group) ? 2 : 1;  // query tiles in this CTA
+    const int h = blockIdx.y;
     const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
     const int tok0 = __ldg(p.cu_seqlens + b);
     const int n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
     const int r0 = qt * BM;
     if (n_new > p.max_new_len) {
-        if (qt == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        if (qt == 0 && h == 0 && threadIdx.x == 0)
             na_report(p.status, NA_ERR_INVALID_ARG);
         return;
     }
@@ -149,6 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (k_begin >= k_end)
         return;
     const int n_tiles = (k_end - k_begin + BN - 1) / BN;
+    const int kvh = h / p.group;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -159,13 +155,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&sm.k_empty[s], 1);
             mbar_init(&sm.v_empty[s], 1);
         }
-        for (int t = 0; t < 2; t++) {
-            mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.s_free[t], 1);
-            mbar_init(&sm.p_full[t], 4);
-            mbar_init(&sm.o_done[t], 1);
+        for (int s = 0; s < NUM_S; s++) {
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.s_free[s], 1);
+            mbar_init(&sm.p_full[s], 4);
         }
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.drain[0], 1);
+        mbar_init(&sm.drain[1], 1);
         sm.abort_flag = 0;
         fence_barrier_init();
     }
@@ -183,10 +180,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc::prefetch_tmap(&map_k);
             tc::prefetch_tmap(&map_v);
             const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
-            mbar_arrive_expect_tx(&sm.q_full, ntile * KB * BM * 128);
-            for (int t = 0; t < ntile; t++)
-                for (int kb = 0; kb < KB; kb++)
-                    tc::tma_load_3d(sm.q[t][kb], &map_q, kb * 64, head0 + t, tok0 + r0, &sm.q_full);
+            mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
+            for (int kb = 0; kb < KB; kb++)
+                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, tok0 + r0, &sm.q_full);
             int issued = 0;
             for (int j = 0; j < n_tiles; j++) {
                 const int st = j % STAGES;
@@ -216,254 +212,263 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issue --
+        // ---------------------------------------------------- S = Q K^T issue --
         if (lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false, false);
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, D, false, true);
             bool ok = mbar_wait_bounded(&sm.q_full, 0);
             bool any = false;
             for (int j = 0; ok && j < n_tiles; j++) {
-                const int st = j % STAGES;
+                const int st = j % STAGES, sb = j % NUM_S;
                 ok = mbar_wait_bounded(&sm.k_full[st], (j / STAGES) & 1);
-                for (int t = 0; ok && t < ntile; t++) {
-                    if (j >= 1)
-                        ok = mbar_wait_bounded(&sm.s_free[t], (j - 1) & 1);
-                    if (!ok || aborted(&sm.abort_flag))
-                        break;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int k = 0; k < D / 16; k++) {
-                        const int kb = k >> 2, kk = k & 3;
-                        const uint64_t a = tc::desc_kmajor_sw128(smem_addr(sm.q[t][kb]) + kk * 32);
-                        const uint64_t bd = tc::desc_kmajor_sw128(smem_addr(sm.k[st][kb]) + kk * 32);
-                        tc::mma_ss(tmem + s_col(t), a, bd, idesc_s, k > 0);
-                    }
-                    tc::mma_commit(&sm.s_full[t]);
-                    any = true;
-                }
+                if (ok && j >= NUM_S)
+                    ok = mbar_wait_bounded(&sm.s_free[sb], ((j / NUM_S) - 1) & 1);
                 if (!ok || aborted(&sm.abort_flag))
                     break;
-                tc::mma_commit(&sm.k_empty[st]);
-                ok = mbar_wait_bounded(&sm.v_full[st], (j / STAGES) & 1);
-                const uint32_t vbase = smem_addr(sm.v[st][0]);
-                for (int t = 0; ok && t < ntile; t++) {
-                    ok = mbar_wait_bounded(&sm.p_full[t], j & 1);
-                    if (!ok || aborted(&sm.abort_flag))
-                        break;
-                    tc::fence_after_sync();
+                tc::fence_after_sync();
+                const uint32_t s_t = tmem + S_COL0 * (sb + 1);
 #pragma unroll
-                    for (int k = 0; k < BN / 16; k++) {
-                        const uint64_t bd = tc::desc_mnmajor_sw128(vbase + k * 16 * 128, BN * 128);
-                        tc::mma_ts(tmem + o_col(t), tmem + s_col(t) + k * 8, bd, idesc_o,
-                                   j > 0 || k > 0);
-                    }
-                    tc::mma_commit(&sm.s_free[t]);
-                    tc::mma_commit(&sm.o_done[t]);
+                for (int k = 0; k < D / 16; k++) {
+                    const int kb = k >> 2, kk = k & 3;
+                    const uint64_t a = tc::desc_kmajor_sw128(smem_addr(sm.q[kb]) + kk * 32);
+                    const uint64_t bd = tc::desc_kmajor_sw128(smem_addr(sm.k[st][kb]) + kk * 32);
+                    tc::mma_ss(s_t, a, bd, idesc_s, k > 0);
                 }
-                if (ok)
-                    tc::mma_commit(&sm.v_empty[st]);
+                tc::mma_commit(&sm.s_full[sb]);
+                tc::mma_commit(&sm.k_empty[st]);
+                any = true;
             }
             if (!ok)
                 set_abort(&sm.abort_flag, p.status);
             if (any) {  // all issued MMAs complete before tensor memory is released
-                tc::mma_commit(&sm.drain);
-                mbar_wait_bounded(&sm.drain, 0);
+                tc::mma_commit(&sm.drain[0]);
+                mbar_wait_bounded(&sm.drain[0], 0);
             }
         }
-    } else {
+    } else if (warp == 2) {
+        // --------------------------------------------------- O += P V issue --
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, D, false, true);
+            bool ok = true, any = false;
+            for (int j = 0; ok && j < n_tiles; j++) {
+                const int st = j % STAGES, sb = j % NUM_S;
+                ok = mbar_wait_bounded(&sm.p_full[sb], (j / NUM_S) & 1);
+                if (ok)
+                    ok = mbar_wait_bounded(&sm.v_full[st], (j / STAGES) & 1);
+                if (!ok || aborted(&sm.abort_flag))
+                    break;
+                tc::fence_after_sync();
+                const uint32_t p_t = tmem + S_COL0 * (sb + 1);
+                const uint32_t vbase = smem_addr(sm.v[st][0]);
+#pragma unroll
+                for (int k = 0; k < BN / 16; k++) {
+                    const uint64_t bd = tc::desc_mnmajor_sw128(vbase + k * 16 * 128, BN * 128);
+                    tc::mma_ts(tmem, p_t + k * 8, bd, idesc_o, j > 0 || k > 0);
+                }
+                tc::mma_commit(&sm.s_free[sb]);
+                tc::mma_commit(&sm.v_empty[st]);
+                tc::mma_commit(&sm.o_done);
+                any = true;
+            }
+            if (!ok)
+                set_abort(&sm.abort_flag, p.status);
+            if (any) {
+                tc::mma_commit(&sm.drain[1]);
+                mbar_wait_bounded(&sm.drain[1], 0);
+            }
+        }
+    } else if (warp >= 4) {
         // ------------------------------------------------------- softmax --
-        const int t = (warp - 2) >> 2;  // query tile of this warpgroup
-        if (t < ntile) {
-            const int quarter = warp & 3;
-            const int r = quarter * 32 + lane;  // query row == TMEM lane
-            const int row_pos = pos_lo + r;
-            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-            const uint32_t s_t = tmem + s_col(t) + lane_off;
-            const uint32_t o_t = tmem + o_col(t) + lane_off;
-            const float sl2 = p.scale_log2;
-            float m_ref = -INFINITY, l = 0.f;
-            bool ok = true;
-            for (int j = 0; j < n_tiles; j++) {
-                const int j0 = k_begin + j * BN;
-                if (!mbar_wait_bounded(&sm.s_full[t], j & 1) || aborted(&sm.abort_flag)) {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // query row == TMEM lane
+        const int row_pos = pos_lo + r;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t o_t = tmem + lane_off;
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; j++) {
+            const int sb = j % NUM_S;
+            const int j0 = k_begin + j * BN;
+            const uint32_t s_t = tmem + S_COL0 * (sb + 1) + lane_off;
+            if (!mbar_wait_bounded(&sm.s_full[sb], (j / NUM_S) & 1) || aborted(&sm.abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                tc::tmem_ld32(s_t + c * 32, sr[c]);
+            tc::tmem_wait_ld();
+
+            const bool need_mask = (j0 + BN - 1 > pos_lo) || (j0 + BN > k_end);
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        const int key = j0 + c * 32 + i;
+                        if (key > row_pos || key >= k_end)
+                            sr[c][i] = __float_as_uint(-INFINITY);
+                    }
+            }
+            // row maximum: four independent chains of 3-input max
+            float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    mxa = max3f(mxa, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                    mxb = max3f(mxb, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
+                    mxc = max3f(mxc, __uint_as_float(sr[c][i + 4]), __uint_as_float(sr[c][i + 5]));
+                    mxd = max3f(mxd, __uint_as_float(sr[c][i + 6]), __uint_as_float(sr[c][i + 7]));
+                }
+            const float mx = max3f(mxa, mxb, fmaxf(mxc, mxd));
+            const float mxs = mx * sl2;
+            float alpha = 1.f;
+            bool corr = false;
+            if (mxs > m_ref + 8.0f) {
+                alpha = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - mxs);
+                corr = (m_ref != -INFINITY);
+                m_ref = mxs;
+            }
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                        sc2, nm2);
+                    float2 pp;
+                    if (c >= 4 - POLY_CHUNKS)
+                        pp = make_float2(exp2_poly(x.x), exp2_poly(x.y));
+                    else
+                        pp = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+                    acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
+                    pk[i] = pack_bf16x2(pp.x, pp.y);
+                }
+                tc::tmem_st16(s_t + c * 16, pk);
+            }
+            const float2 acc01 = __fadd2_rn(acc[0], acc[1]), acc23 = __fadd2_rn(acc[2], acc[3]);
+            const float rs = (acc01.x + acc01.y) + (acc23.x + acc23.y);
+            tc::tmem_wait_st();
+
+            if (j0 + BN > k_end) {
+                // Key rows past the valid range hold whatever the cache has there;
+                // zero them so P * V sees no non-finite values.
+                const int st = j % STAGES;
+                if (!mbar_wait_bounded(&sm.v_full[st], (j / STAGES) & 1)) {
                     ok = false;
                     break;
                 }
+                if (r >= k_end - j0) {
+#pragma unroll
+                    for (int kb = 0; kb < KB; kb++) {
+                        uint4 *row = reinterpret_cast<uint4 *>(sm.v[st][kb] + r * 64);
+#pragma unroll
+                        for (int c = 0; c < 8; c++)
+                            row[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                tc::fence_proxy_async_smem();
+            }
+            // Wait for PV(j-1) on every tile: the parity wait is only exact while
+            // the waiter is at most one phase behind the barrier, and up to two
+            // PVs can be in flight here.
+            if (j >= 1 && !mbar_wait_bounded(&sm.o_done, (j - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, corr)) {
+                // rescale this warp's O rows (PV(j-1) has landed)
                 tc::fence_after_sync();
-                uint32_t sr[4][32];
+                const float a = corr ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < 4; c++)
-                    tc::tmem_ld32(s_t + c * 32, sr[c]);
-                tc::tmem_wait_ld();
-
-                const bool need_mask = (j0 + BN - 1 > pos_lo) || (j0 + BN > k_end);
-                if (need_mask) {
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(o_t + c * 32, o);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 4; c++)
-#pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            const int key = j0 + c * 32 + i;
-                            if (key > row_pos || key >= k_end)
-                                sr[c][i] = __float_as_uint(-INFINITY);
-                        }
+                    for (int i = 0; i < 32; i++)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                    tc::tmem_st32(o_t + c * 32, o);
                 }
-                // row maximum: four independent chains of 3-input max
-                float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 4; c++)
-#pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        mxa = max3f(mxa, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
-                        mxb = max3f(mxb, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
-                        mxc = max3f(mxc, __uint_as_float(sr[c][i + 4]), __uint_as_float(sr[c][i + 5]));
-                        mxd = max3f(mxd, __uint_as_float(sr[c][i + 6]), __uint_as_float(sr[c][i + 7]));
-                    }
-                const float mx = max3f(mxa, mxb, fmaxf(mxc, mxd));
-                const float mxs = mx * sl2;
-                float alpha = 1.f;
-                bool corr = false;
-                if (mxs > m_ref + 8.0f) {
-                    alpha = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - mxs);
-                    corr = (m_ref != -INFINITY);
-                    m_ref = mxs;
-                }
-                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
-                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                 make_float2(0.f, 0.f)};
-#pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
-                            sc2, nm2);
-                        float2 pp;
-                        if (c >= 4 - POLY_CHUNKS)
-                            pp = make_float2(exp2_poly(x.x), exp2_poly(x.y));
-                        else
-                            pp = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-                        acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
-                        pk[i] = pack_bf16x2(pp.x, pp.y);
-                    }
-                    tc::tmem_st16(s_t + c * 16, pk);
-                }
-                const float2 acc01 = __fadd2_rn(acc[0], acc[1]), acc23 = __fadd2_rn(acc[2], acc[3]);
-                const float rs = (acc01.x + acc01.y) + (acc23.x + acc23.y);
                 tc::tmem_wait_st();
-
-                if (t == 0 && j0 + BN > k_end) {
-                    // Key rows past the valid range hold whatever the cache has
-                    // there; zero them so P * V sees no non-finite values.
-                    const int st = j % STAGES;
-                    if (!mbar_wait_bounded(&sm.v_full[st], (j / STAGES) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    if (r >= k_end - j0) {
-#pragma unroll
-                        for (int kb = 0; kb < KB; kb++) {
-                            uint4 *row = reinterpret_cast<uint4 *>(sm.v[st][kb] + r * 64);
-#pragma unroll
-                            for (int c = 0; c < 8; c++)
-                                row[c] = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    tc::fence_proxy_async_smem();
-                }
-                if (j >= 1 && __any_sync(0xffffffffu, corr)) {
-                    // rescale this warp's O rows once PV(j-1) has landed
-                    if (!mbar_wait_bounded(&sm.o_done[t], (j - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    const float a = corr ? alpha : 1.f;
-#pragma unroll
-                    for (int c = 0; c < D / 32; c++) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(o_t + c * 32, o);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; i++)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                        tc::tmem_st32(o_t + c * 32, o);
-                    }
-                    tc::tmem_wait_st();
-                }
-                l = l * alpha + rs;
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.p_full[t]);
             }
-            if (!ok) {
-                if (lane == 0)
-                    set_abort(&sm.abort_flag, p.status);
-            } else if (mbar_wait_bounded(&sm.o_done[t], (n_tiles - 1) & 1)) {
-                // -------------------------------------------------- epilogue --
-                tc::fence_after_sync();
-                const size_t tok = (size_t)(tok0 + r0 + r);
-                const int h = head0 + t;
-                const bool valid = r < rows;
-                if (p.num_splits == 1) {
-                    const float inv = l > 0.f ? 1.0f / l : 0.f;
-                    bf16 *dst = p.out + (tok * p.H + h) * D;
-                    const bool gated = (p.flags & NA_OUT_GATE) && p.gate;
-#pragma unroll
-                    for (int c = 0; c < D / 32; c++) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(o_t + c * 32, o);
-                        tc::tmem_wait_ld();
-                        if (!valid)
-                            continue;
-                        float f[32];
-#pragma unroll
-                        for (int i = 0; i < 32; i++)
-                            f[i] = __uint_as_float(o[i]) * inv;
-                        if (gated) {
-                            const uint4 *g4 =
-                                reinterpret_cast<const uint4 *>(p.gate + (tok * p.H + h) * D + c * 32);
-#pragma unroll
-                            for (int q = 0; q < 4; q++) {
-                                float g[8];
-                                bf16x8_to_f32(__ldg(g4 + q), g);
-#pragma unroll
-                                for (int e = 0; e < 8; e++)
-                                    f[q * 8 + e] *= 1.0f / (1.0f + __expf(-g[e]));
-                            }
-                        }
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-#pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            d4[q] = f32_to_bf16x8(f + q * 8);
-                    }
-                } else {
-                    const size_t row = (tok * p.H + h) * p.num_splits + split;
-                    float *dst = p.part_o + row * D;
-#pragma unroll
-                    for (int c = 0; c < D / 32; c++) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(o_t + c * 32, o);
-                        tc::tmem_wait_ld();
-                        if (!valid)
-                            continue;
-                        float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
-#pragma unroll
-                        for (int q = 0; q < 8; q++)
-                            d4[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                                __uint_as_float(o[4 * q + 2]),
-                                                __uint_as_float(o[4 * q + 3]));
-                    }
-                    if (valid) {
-                        p.part_ml[row * 2] = m_ref;
-                        p.part_ml[row * 2 + 1] = l;
-                    }
-                }
-            } else if (lane == 0) {
+            l = l * alpha + rs;
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.p_full[sb]);
+        }
+        if (!ok) {
+            if (lane == 0)
                 set_abort(&sm.abort_flag, p.status);
+        } else if (mbar_wait_bounded(&sm.o_done, (n_tiles - 1) & 1)) {
+            // ---------------------------------------------------- epilogue --
+            tc::fence_after_sync();
+            const size_t tok = (size_t)(tok0 + r0 + r);
+            const bool valid = r < rows;
+            if (p.num_splits == 1) {
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+                bf16 *dst = p.out + (tok * p.H + h) * D;
+                const bool gated = (p.flags & NA_OUT_GATE) && p.gate;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(o_t + c * 32, o);
+                    tc::tmem_wait_ld();
+                    if (!valid)
+                        continue;
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        f[i] = __uint_as_float(o[i]) * inv;
+                    if (gated) {
+                        const uint4 *g4 =
+                            reinterpret_cast<const uint4 *>(p.gate + (tok * p.H + h) * D + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            float g[8];
+                            bf16x8_to_f32(__ldg(g4 + q), g);
+#pragma unroll
+                            for (int e = 0; e < 8; e++)
+                                f[q * 8 + e] *= 1.0f / (1.0f + __expf(-g[e]));
+                        }
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        d4[q] = f32_to_bf16x8(f + q * 8);
+                }
+            } else {
+                const size_t row = (tok * p.H + h) * p.num_splits + split;
+                float *dst = p.part_o + row * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(o_t + c * 32, o);
+                    tc::tmem_wait_ld();
+                    if (!valid)
+                        continue;
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; q++)
+                        d4[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                            __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+                }
+                if (valid) {
+                    p.part_ml[row * 2] = m_ref;
+                    p.part_ml[row * 2 + 1] = l;
+                }
             }
+        } else if (lane == 0) {
+            set_abort(&sm.abort_flag, p.status);
         }
     }
 
@@ -595,7 +600,7 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
             return e;
         configured = true;
     }
-    dim3 grid(p.q_tiles, p.KV * ((p.group + 1) / 2), p.batch * p.num_splits);
+    dim3 grid(p.q_tiles, p.H, p.batch * p.num_splits);
     prefill_tc_kernel<D><<<grid, THREADS, smem, stream>>>(p, mq, mk, mv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1)
