@@ -21,9 +21,10 @@
 //   warps 4-7  softmax, one query row per thread (its TMEM lane): load S_j,
 //              mask, online max in the log2 domain (the reference max is raised
 //              only when it grows by more than 2^8, and only then is the O row
-//              rescaled in tensor memory), exponentiate (a quarter on the FMA
-//              pipe, exp2_poly, the rest on MUFU), write P_j as bf16 over S_j,
-//              and finally normalise, gate and store O.
+//              rescaled in tensor memory), exponentiate on the MUFU unit
+//              (measured faster than moving part of the exponentials to a
+//              polynomial on the FMA pipe), write P_j as bf16 over S_j, and
+//              finally normalise, gate and store O.
 // With three S buffers the tensor core computes S_{j+1} and S_{j+2} while the
 // softmax works on tile j, and PV_j runs while it prepares P_{j+1}.
 //
@@ -42,7 +43,6 @@ constexpr int NUM_S = 3;     // S/P buffers in tensor memory
 constexpr int THREADS = 256; // 8 warps: producer, S issuer, PV issuer, idle, 4 softmax
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL0 = 128;  // S buffer i at columns 128 (i + 1); O at column 0
-constexpr int POLY_CHUNKS = 1;    // 32-column chunks of each S row exponentiated on the FMA pipe
 
 template <int D>
 struct __align__(1024) TcSmem {
@@ -71,21 +71,6 @@ __device__ __forceinline__ void set_abort(int *flag, int32_t *status)
 {
     *(volatile int *)flag = 1;
     na_report(status, NA_ERR_DEVICE_TIMEOUT);
-}
-
-// 2^x on the FMA pipe: x = n + f with n = floor(x), f in [0, 1); 2^f from a
-// degree-3 polynomial (weighted least-squares fit of 2^f on [0, 1) for minimum
-// relative error, max 7.5e-5 = 2^-13.7, far below the bf16 rounding P takes
-// next); 2^n added to the exponent field.  Arguments below -126 give 0.
-__device__ __forceinline__ float exp2_poly(float x)
-{
-    const float fl = floorf(x);
-    const float f = x - fl;
-    const float p = fmaf(fmaf(fmaf(0.07802451680313915f, f, 0.2260671637365104f), f,
-                              0.6958335376411953f),
-                         f, 0.9999252186969307f);
-    const float r = __int_as_float(__float_as_int(p) + ((int)fl << 23));
-    return x < -126.0f ? 0.0f : r;
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c)
@@ -344,11 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const float2 x = __ffma2_rn(
                         make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
                         sc2, nm2);
-                    float2 pp;
-                    if (c >= 4 - POLY_CHUNKS)
-                        pp = make_float2(exp2_poly(x.x), exp2_poly(x.y));
-                    else
-                        pp = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+                    const float2 pp = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
                     acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
                     pk[i] = pack_bf16x2(pp.x, pp.y);
                 }
