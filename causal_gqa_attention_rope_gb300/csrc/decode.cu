@@ -4,14 +4,23 @@
 // fn attend_all_heads: each KV group's keys and values are streamed once for
 // all of its query heads).
 //
-// Split pass (persistent, one CTA per SM).  A work unit is (split, sequence,
-// kv head, head chunk): up to `split_len` consecutive keys of one KV head, for
-// HPC query heads of its group.  One producer lane streams the unit's key and
-// value tiles (DEC_TILE keys, contiguous in the head-major cache) into a
-// DEC_STAGES-deep shared-memory ring with 1-D bulk async copies completing on
-// mbarriers; eight consumer warps score and accumulate.  Scores never touch
-// tensor cores: per key the group does 2 * HPC * d flops over 4 d bytes, far
-// below the SIMT rate, so the pass is bound by HBM bandwidth.
+// Split pass (persistent, two CTAs per SM).  The keys to read form S streams,
+// one per (sequence, kv head, head chunk) -- a head chunk being the HPC query
+// heads of a KV group that one CTA scores together -- laid end to end in
+// sequence-major order.  CTA c takes the contiguous slice [c P, (c + 1) P) of
+// that concatenation, P = max(ceil(total / grid), min_slice): every CTA reads
+// the same number of keys whatever the mix of sequence lengths, so none idles
+// while others finish long sequences.  A slice cuts streams into pieces; the
+// piece of stream s in CTA c gets the id s + c, unique and consecutive along a
+// stream, and its partial output lands in workspace row id.  The CTA holding a
+// stream's first (last) key records that piece id for the combine pass.
+//
+// In each CTA one producer lane streams the piece's key and value tiles
+// (DEC_TILE keys, contiguous in the head-major cache) into a DEC_STAGES-deep
+// shared-memory ring with 1-D bulk async copies completing on mbarriers;
+// seven consumer warps score and accumulate.  Scores never touch tensor cores:
+// per key the group does 2 * HPC * d flops over 4 d bytes, far below the SIMT
+// rate, so the pass is bound by HBM bandwidth.
 //
 // Consumer lane layout: a warp takes 2 keys per step (key group kg = lane / 16);
 // the 16 lanes of a key group split head_dim into slices of d/16 elements.
@@ -21,7 +30,10 @@
 // exceeds it by more than 2^8 (factor 256), so the accumulator rescale runs a
 // handful of times per split instead of per tile; scores are carried in the
 // log2 domain (q pre-scaled by scale * log2 e).  Two CTAs share an SM (about
-// 112 KB of shared memory and <= 112 registers per thread each).
+// 100 KB of shared memory each).  Eight warps per CTA keep four warps per SM
+// sub-partition, so each thread may hold 128 registers: the d = 128, four-head
+// instance needs 127 and spilled to local memory under the 96-register cap
+// that nine-warp CTAs impose (measured 22% slower).
 //
 // Raw log2-domain scores are written to the probability buffer; the combine
 // pass turns them into probabilities once the global maximum and sum are known,
@@ -30,13 +42,30 @@
 
 namespace {
 
-constexpr int DEC_TILE = 64;
+constexpr int DEC_TILE = 56;  // DEC_CWARPS warps x 8 keys
 constexpr int DEC_STAGES = 3;
-constexpr int DEC_CWARPS = 8;
+constexpr int DEC_CWARPS = 7;
 constexpr int DEC_THREADS = (DEC_CWARPS + 1) * 32;
 constexpr int LPK = 16;                    // lanes per key
 constexpr int KPS = 32 / LPK;              // keys per warp step
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+
+// Keys of sequence b, or 0 for a length past the cache capacity or the host
+// bound (skipped here, reported by the combine pass).
+__device__ __forceinline__ int valid_len(const DecodeParams &p, int b)
+{
+    const int n = __ldg(p.kv_lens + b);
+    return (n < 0 || n > p.capacity || n > p.max_kv_len) ? 0 : n;
+}
+
+// Where this CTA's key slice starts: computed by one full warp, then shared.
+struct Slice {
+    long long start, end;  // [start, end) in the concatenation of all streams
+    long long off;         // offset of the stream holding `start`
+    int b, si;             // its sequence and stream index within the sequence
+    int empty;
+};
 
 template <int D, int HPC>
 struct DecSmem {
@@ -47,35 +76,114 @@ struct DecSmem {
     float merge_l[DEC_CWARPS][HPC];
     uint64_t full[DEC_STAGES];
     uint64_t empty[DEC_STAGES];
+    Slice slice;
     int abort_flag;
 };
 
-struct Unit {
-    int split, b, kvh, hc;
+// One piece: the keys [k0, k1) of stream (b, kvh, hc) that this CTA reads.
+struct Piece {
+    int b, kvh, hc, k0, k1, id;
+    bool first, last;  // holds the stream's first / last key
 };
 
-__device__ __forceinline__ Unit unit_of(int u, const DecodeParams &p)
+__device__ __forceinline__ void locate_slice(const DecodeParams &p, int lane, Slice &out)
 {
-    Unit r;
-    r.hc = u % p.head_chunks;
-    u /= p.head_chunks;
-    r.kvh = u % p.KV;
-    u /= p.KV;
-    r.b = u % p.batch;
-    r.split = u / p.batch;
-    return r;
+    const unsigned FULL = 0xffffffffu;
+    const int spb = p.KV * p.head_chunks;  // streams per sequence
+    long long t = 0;
+    for (int b = lane; b < p.batch; b += 32)
+        t += valid_len(p, b);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        t += __shfl_xor_sync(FULL, t, m);
+    const long long total = t * spb;
+    const long long grid = gridDim.x;
+    long long P = (total + grid - 1) / grid;
+    if (P < p.min_slice)
+        P = p.min_slice;
+    Slice sl{};
+    sl.start = (long long)blockIdx.x * P;
+    sl.end = min(sl.start + P, total);
+    sl.empty = sl.start >= total;
+    if (!sl.empty) {
+        // First sequence whose streams extend past `start`.
+        long long base = 0;
+        for (int b0 = 0; b0 < p.batch; b0 += 32) {
+            const int b = b0 + lane;
+            const int n = b < p.batch ? valid_len(p, b) : 0;
+            const long long w = (long long)n * spb;
+            long long incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            const long long excl = base + incl - w;
+            const unsigned hit = __ballot_sync(FULL, w > 0 && sl.start < excl + w && sl.start >= excl);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                sl.b = b0 + src;
+                const long long off_b = __shfl_sync(FULL, excl, src);
+                const int nb = __shfl_sync(FULL, n, src);
+                sl.si = (int)((sl.start - off_b) / nb);
+                sl.off = off_b + (long long)sl.si * nb;
+                break;
+            }
+            base += __shfl_sync(FULL, incl, 31);
+        }
+    }
+    if (lane == 0)
+        out = sl;
 }
 
-// Key range [s0, s1) of a unit; empty when s0 >= s1.  Lengths past the cache
-// capacity or the host bound are skipped here and reported by the combine pass.
-__device__ __forceinline__ void unit_keys(const Unit &w, const DecodeParams &p, int &s0, int &s1)
-{
-    const int n = __ldg(p.kv_lens + w.b);
-    s0 = w.split * p.split_len;
-    s1 = min(n, s0 + p.split_len);
-    if (n < 0 || n > p.capacity || n > p.max_kv_len)
-        s1 = s0;
-}
+// Walks this CTA's pieces in order; every thread of the CTA walks the same way.
+struct Walker {
+    long long start, end, off;
+    int b, si, len, spb, c;
+    bool done;
+
+    __device__ __forceinline__ void init(const Slice &sl, const DecodeParams &p)
+    {
+        start = sl.start;
+        end = sl.end;
+        off = sl.off;
+        b = sl.b;
+        si = sl.si;
+        spb = p.KV * p.head_chunks;
+        c = blockIdx.x;
+        done = sl.empty != 0;
+        len = done ? 0 : valid_len(p, b);
+    }
+
+    __device__ __forceinline__ bool next(const DecodeParams &p, Piece &pc)
+    {
+        while (!done && b < p.batch && off < end) {
+            const long long s_off = off;
+            const int n = len, sb = b, ssi = si;
+            off += n;
+            if (++si == spb) {
+                si = 0;
+                if (++b < p.batch)
+                    len = valid_len(p, b);
+            }
+            const long long lo = start > s_off ? start - s_off : 0;
+            const long long hi = end - s_off < n ? end - s_off : n;
+            if (lo < hi) {
+                pc.b = sb;
+                pc.kvh = ssi / p.head_chunks;
+                pc.hc = ssi - pc.kvh * p.head_chunks;
+                pc.k0 = (int)lo;
+                pc.k1 = (int)hi;
+                pc.id = sb * spb + ssi + c;
+                pc.first = lo == 0;
+                pc.last = hi == n;
+                return true;
+            }
+        }
+        return false;
+    }
+};
 
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
 {
@@ -115,7 +223,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
         sm.abort_flag = 0;
         fence_barrier_init();
     }
+    if (warp == DEC_CWARPS)
+        locate_slice(p, lane, sm.slice);
     __syncthreads();
+    Walker walk;
+    walk.init(sm.slice, p);
+    Piece pc;
 
     const size_t cap = (size_t)p.capacity;
 
@@ -126,11 +239,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
         const uint64_t policy = l2_policy_evict_first();
         uint32_t it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
-            const Unit w = unit_of(u, p);
-            int s0, s1;
-            unit_keys(w, p, s0, s1);
-            const size_t head_base = ((size_t)w.b * p.KV + w.kvh) * cap * D;
+        while (ok && walk.next(p, pc)) {
+            const int s0 = pc.k0, s1 = pc.k1;
+            const size_t head_base = ((size_t)pc.b * p.KV + pc.kvh) * cap * D;
             for (int j0 = s0; j0 < s1; j0 += DEC_TILE, it++) {
                 const int stage = it % DEC_STAGES;
                 const uint32_t parity = ((it / DEC_STAGES) & 1) ^ 1;
@@ -169,25 +280,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
     const int hsel = sub / R;      // head whose score this lane ends up holding
     const unsigned FULL = 0xffffffffu;
     uint32_t it = 0;
-    // A warp whose wait timed out keeps walking the units so that every warp
+    // A warp whose wait timed out keeps walking the pieces so that every warp
     // joins the same named barriers, but does no more waits or writes.
     bool aborted = false;
 
-    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-        const Unit w = unit_of(u, p);
-        int s0, s1;
-        unit_keys(w, p, s0, s1);
-        if (s0 >= s1)
-            continue;
+    while (walk.next(p, pc)) {
+        const int s0 = pc.k0, s1 = pc.k1;
         if (*(volatile int *)&sm.abort_flag)
             aborted = true;
-        const int head0 = w.kvh * p.group + w.hc * HPC;
+        const int head0 = pc.kvh * p.group + pc.hc * HPC;
 
         float2 q[HPC][EPL / 2];
 #pragma unroll
         for (int h = 0; h < HPC; h++) {
             uint32_t wd[EPL / 2];
-            load_words<EPL / 2>(p.q + ((size_t)w.b * p.H + head0 + h) * D + sub * EPL, wd);
+            load_words<EPL / 2>(p.q + ((size_t)pc.b * p.H + head0 + h) * D + sub * EPL, wd);
 #pragma unroll
             for (int e = 0; e < EPL / 2; e++) {
                 const float2 f = bf16x2_to_f2(wd[e]);
@@ -204,7 +311,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
                 acc[h][e] = make_float2(0.f, 0.f);
         }
         float l_lane = 0.f;
-        float *probs_row = p.probs ? p.probs + ((size_t)w.b * p.H + head0 + hsel) * p.probs_stride
+        float *probs_row = p.probs ? p.probs + ((size_t)pc.b * p.H + head0 + hsel) * p.probs_stride
                                    : nullptr;
 
         for (int j0 = s0; j0 < s1 && !aborted; j0 += DEC_TILE, it++) {
@@ -377,12 +484,19 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
             }
             if (aborted)
                 continue;
-            const size_t row = ((size_t)w.b * p.H + head0 + h) * p.max_splits + w.split;
+            const size_t row = (size_t)pc.id * HPC + h;
             p.part_o[row * D + e] = o;
             if (e == 0) {
                 p.part_ml[row * 2] = M;
                 p.part_ml[row * 2 + 1] = l;
             }
+        }
+        if (threadIdx.x == 0 && !aborted) {
+            const int stream = pc.id - blockIdx.x;
+            if (pc.first)
+                p.piece_span[2 * stream] = pc.id;
+            if (pc.last)
+                p.piece_span[2 * stream + 1] = pc.id;
         }
         named_barrier_sync(1, DEC_CWARPS * 32);
     }
@@ -408,20 +522,34 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
             out[e] = __float2bfloat16_rn(0.f);
         return;
     }
-    const int ns = (n + p.split_len - 1) / p.split_len;
-    const float *ml = p.part_ml + (size_t)bh * p.max_splits * 2;
+    // Pieces of this head's stream: ids first..last, HPC heads per row group.
+    const int h = bh - b * p.H;
+    const int hpc = p.group / p.head_chunks;
+    const int kvh = h / p.group, r = h - kvh * p.group;
+    const int stream = (b * p.KV + kvh) * p.head_chunks + r / hpc;
+    const int first = p.piece_span[2 * stream], last = p.piece_span[2 * stream + 1];
+    if (first < 0 || last < first || last >= p.max_pieces) {  // the split pass gave up
+        if (threadIdx.x == 0)
+            na_report(p.status, NA_ERR_DEVICE_TIMEOUT);
+        for (int e = threadIdx.x; e < D; e += blockDim.x)
+            out[e] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const int ns = last - first + 1;
+    const size_t row0 = (size_t)first * hpc + (r % hpc);
+    const float *ml = p.part_ml + row0 * 2;
     float M = -INFINITY;
     for (int s = 0; s < ns; s++)
-        M = fmaxf(M, ml[2 * s]);
+        M = fmaxf(M, ml[2 * hpc * s]);
     float L = 0.f;
     for (int s = 0; s < ns; s++)
-        L += ml[2 * s + 1] * exp2f(ml[2 * s] - M);
+        L += ml[2 * hpc * s + 1] * exp2f(ml[2 * hpc * s] - M);
     const float inv_l = 1.0f / L;
-    const float *po = p.part_o + (size_t)bh * p.max_splits * D;
+    const float *po = p.part_o + row0 * D;
     for (int e = threadIdx.x; e < D; e += blockDim.x) {
         float o = 0.f;
         for (int s = 0; s < ns; s++)
-            o += po[(size_t)s * D + e] * exp2f(ml[2 * s] - M);
+            o += po[(size_t)s * hpc * D + e] * exp2f(ml[2 * hpc * s] - M);
         o *= inv_l;
         if ((p.flags & NA_OUT_GATE) && p.gate) {
             const float g = __bfloat162float(p.gate[(size_t)bh * D + e]);
@@ -467,12 +595,7 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
             return e;
         configured = true;
     }
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = p.total_units < 2 * sms ? p.total_units : 2 * sms;  // two CTAs per SM
-    if (grid > 0)
-        decode_split_kernel<D, HPC><<<grid, DEC_THREADS, smem, stream>>>(p);
+    decode_split_kernel<D, HPC><<<p.grid, DEC_THREADS, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -483,6 +606,8 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
 }  // namespace
 
 int decode_key_tile() { return DEC_TILE; }
+
+int decode_ctas_per_sm() { return 2; }
 
 cudaError_t launch_decode(const DecodeParams &p, int d, int heads_per_cta, cudaStream_t stream)
 {

@@ -146,10 +146,14 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
 }
 
 struct DecodePlan {
-    int split_len, max_splits, heads_per_cta;
+    int heads_per_cta, grid, min_slice, max_pieces, streams;
     size_t ws_bytes;
 };
 
+// Decode split plan.  The split pass runs a fixed grid (two CTAs per SM) and
+// cuts the concatenated key streams into one equal slice per CTA (at least
+// min_slice keys), so the workspace holds one partial row group per piece:
+// streams + grid pieces at most, whatever the lengths.
 DecodePlan plan_decode(const na_attn_cfg *c, int batch, int max_kv_len, int num_splits)
 {
     DecodePlan pl{};
@@ -157,21 +161,16 @@ DecodePlan plan_decode(const na_attn_cfg *c, int batch, int max_kv_len, int num_
     const int group = c->num_heads / c->num_kv_heads;
     pl.heads_per_cta = (group % 4 == 0) ? 4 : ((group % 2 == 0) ? 2 : 1);
     const int len = max_kv_len > 0 ? max_kv_len : 1;
-    int split_len;
-    if (num_splits > 0) {
-        split_len = (len + num_splits - 1) / num_splits;
-    } else {
-        // Keys per unit: 512 by default; longer when the batch alone gives
-        // every SM several units.
-        const long long units_per_split = (long long)batch * c->num_kv_heads * (group / pl.heads_per_cta);
-        split_len = 512;
-        while (split_len < len && units_per_split * ((len + split_len - 1) / split_len) > 64ll * sm_count())
-            split_len *= 2;
-    }
-    split_len = (split_len + tile - 1) / tile * tile;
-    pl.split_len = split_len;
-    pl.max_splits = (len + split_len - 1) / split_len;
-    pl.ws_bytes = (size_t)batch * c->num_heads * pl.max_splits * (c->head_dim + 2) * 4;
+    int min_slice = num_splits > 0 ? (len + num_splits - 1) / num_splits : 4 * tile;
+    if (min_slice < 1)
+        min_slice = 1;
+    pl.min_slice = min_slice;
+    pl.grid = decode_ctas_per_sm() * sm_count();
+    pl.streams = batch * c->num_kv_heads * (group / pl.heads_per_cta);
+    pl.max_pieces = pl.streams + pl.grid;
+    const size_t rows = (size_t)pl.max_pieces * pl.heads_per_cta;
+    pl.ws_bytes = rows * (c->head_dim + 2) * 4 + (size_t)pl.streams * 2 * 4;
+    pl.ws_bytes = (pl.ws_bytes + 15) / 16 * 16;
     return pl;
 }
 
@@ -370,10 +369,10 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     p.batch = batch;
     p.capacity = cache->capacity;
     p.scale_log2 = score_scale_log2(cfg);
-    p.split_len = pl.split_len;
-    p.max_splits = pl.max_splits;
     p.head_chunks = p.group / pl.heads_per_cta;
-    p.total_units = batch * p.KV * p.head_chunks * pl.max_splits;
+    p.grid = pl.grid;
+    p.min_slice = pl.min_slice;
+    p.max_pieces = pl.max_pieces;
     p.max_kv_len = max_kv_len;
     p.flags = cfg->flags;
     p.q = static_cast<const bf16 *>(q_rot);
@@ -385,7 +384,9 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     p.probs = probs;
     p.probs_stride = probs ? probs_stride : 0;
     p.part_o = static_cast<float *>(workspace);
-    p.part_ml = p.part_o + (size_t)batch * p.H * pl.max_splits * cfg->head_dim;
+    const size_t rows = (size_t)pl.max_pieces * pl.heads_per_cta;
+    p.part_ml = p.part_o + rows * cfg->head_dim;
+    p.piece_span = reinterpret_cast<int32_t *>(p.part_ml + rows * 2);
     p.status = status;
     return launch_decode(p, cfg->head_dim, pl.heads_per_cta, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess

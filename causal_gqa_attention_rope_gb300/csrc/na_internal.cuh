@@ -167,10 +167,10 @@ struct RopeAppendParams {
 struct DecodeParams {
     int H, KV, group, batch, capacity;
     float scale_log2;          // score scale * log2(e)
-    int split_len;             // keys per split (multiple of the key tile)
-    int max_splits;            // splits per (sequence, head) in the workspace layout
     int head_chunks;           // group / heads-per-CTA
-    int total_units;           // batch * KV * head_chunks * max_splits
+    int grid;                  // CTAs of the split pass, one key slice each
+    int min_slice;             // fewest keys in a CTA's slice
+    int max_pieces;            // streams + grid: bound on piece ids
     int max_kv_len;            // host bound on kv_lens (checked on the device)
     uint32_t flags;
     const bf16 *q, *cache_k, *cache_v, *gate;
@@ -178,8 +178,9 @@ struct DecodeParams {
     bf16 *out;
     float *probs;
     long long probs_stride;
-    float *part_o;             // [B][H][max_splits][d]
-    float *part_ml;            // [B][H][max_splits][2]  (max, sum) in the log2 domain
+    float *part_o;             // [max_pieces][heads-per-CTA][d]
+    float *part_ml;            // [max_pieces][heads-per-CTA][2]  (max, sum) in the log2 domain
+    int32_t *piece_span;       // [streams][2]  first and last piece id of each stream
     int32_t *status;
 };
 
@@ -208,5 +209,6 @@ cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, int 
                            cudaStream_t stream);
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd);
 int decode_key_tile();
+int decode_ctas_per_sm();
 int prefill_key_tile();
 int prefill_q_tile();

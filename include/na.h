@@ -159,8 +159,15 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
  *   out        bf16 [batch][H][d].
  *   probs      fp32 [batch][H][probs_stride] or NULL: probs[b][h][j] = p_j for
  *              j < kv_lens[b]; entries past kv_lens[b] are not written.
- *   num_splits KV splits per sequence (0 = choose automatically from the SM count).
- *   workspace  at least na_decode_workspace_size() bytes.
+ *   num_splits granularity of the key split (0 = automatic).  The keys of all
+ *              sequences are cut into one equal slice per CTA of the split pass
+ *              (two CTAs per SM); num_splits > 0 makes every slice at least
+ *              ceil(max_kv_len / num_splits) keys long, so the longest sequence
+ *              is merged from at most num_splits + 1 partial results.
+ *   workspace  at least na_decode_workspace_size() bytes: partial results of
+ *              every slice piece plus 8 bytes per (sequence, kv head, head
+ *              chunk); its size depends on the batch and the head layout, not on
+ *              the lengths.  Not read before the call writes it.
  */
 int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
                    const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
@@ -182,8 +189,7 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
  *
  *   - Sizes whose na_decode_workspace_size() exceeds 20 MiB are rejected with
  *     NA_ERR_WORKSPACE before anything is enqueued (for 32 query heads and
- *     head_dim 128: batch * max_kv_len up to about 640K keys with the automatic
- *     split choice).
+ *     head_dim 128: a batch of up to about 1200 sequences, of any length).
  *   - The first call on a device looks up the array's device address (with that
  *     device current); make that first call before any stream capture.
  *   - All calls share the array and it keeps the last call's contents; the

@@ -54,6 +54,15 @@ def test_decode_forced_splits(oracle, splits):
     _check(oracle, dec, num_splits=splits)
 
 
+@pytest.mark.parametrize("splits", [0, 40])
+def test_decode_balanced_slices_skip_empty_sequences(oracle, splits):
+    """Key slices that start inside runs of empty sequences, a batch wider than
+    one warp's scan, and one long sequence cut across many slices."""
+    lens = [0] * 37 + [3000] + [1, 0] * 15 + [0, 257, 0]
+    dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128), lens, 3072, seed=93)
+    _check(oracle, dec, num_splits=splits)
+
+
 def test_decode_without_probs(oracle):
     dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128, out_gate=True), [300, 64], 512, seed=91)
     _check(oracle, dec, with_probs=False)
