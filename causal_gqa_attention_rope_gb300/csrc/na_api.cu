@@ -110,10 +110,11 @@ struct PrefillPlan {
 };
 
 // Split the keys across CTAs only when the (query tile, head, sequence)
-// grid would leave most SMs idle (one CTA owns an SM); the split count targets
-// about one CTA per SM, each split covering at least four key tiles (fewer,
-// longer splits measured faster than more, shorter ones: less partial traffic
-// for the combine pass).
+// grid would leave most SMs idle (one CTA owns an SM).  The split count keeps
+// the grid within one wave (est * splits <= SMs: a 5-way split of 32 tiles on
+// 152 SMs left 8 CTAs for a second wave and measured ~2x slower than 4-way),
+// each split covering at least four key tiles (fewer, longer splits measured
+// faster than more, shorter ones: less partial traffic for the combine pass).
 PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int max_new_len,
                          int max_total_len)
 {
@@ -124,7 +125,7 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     const long long target = sm_count();
     int splits = 1;
     if (est < target && max_total_len > 4 * bn) {
-        splits = (int)((target + est - 1) / est);
+        splits = (int)(target / est);
         const int max_by_len = (max_total_len + 4 * bn - 1) / (4 * bn);
         splits = splits < max_by_len ? splits : max_by_len;
         if (splits < 1)
