@@ -214,7 +214,8 @@ int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_
         return NA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out))
         return NA_ERR_INVALID_ARG;
-    if ((cfg->flags & NA_QK_NORM) && (!q_norm_w || !k_norm_w))
+    if ((cfg->flags & NA_QK_NORM) &&
+        (!q_norm_w || !k_norm_w || !aligned16(q_norm_w) || !aligned16(k_norm_w)))
         return NA_ERR_INVALID_ARG;
     if (rope_append_smem_bytes(cfg->num_heads, cfg->num_kv_heads, cfg->head_dim,
                                cfg->rotary_dim) > 200 * 1024)

@@ -9,39 +9,192 @@
 // rope_rotate_scaled (half-split pairs (x[i], x[i + rd/2]), both outputs scaled
 // by the attention factor).
 //
-// One CTA per token.  The token's H + 2 KV rows (a few KB, contiguous in q, k
-// and v) are read with 16-byte loads, staged in shared memory as fp32, normed
-// and rotated by one warp per row, and written back with 16-byte stores: q_out
-// contiguously, K and V into their head-major cache slots.  The kernel is bound
-// by HBM traffic: 2 * (H + 2 KV) * d * 2 bytes per token.
+// One CTA per token; the kernel moves 2 * (H + 2 KV) * d * 2 bytes per token
+// and, at a few hundred tokens per call, is bound by the latency of that one
+// round trip.  So everything the token needs is requested first, and the work
+// between the loads and the stores is short and free of double precision:
+//   - rope_append_kernel (rotary_dim a multiple of 16): each thread owns one
+//     32-byte unit of a row -- chunks [8k, 8k + 8) and [rd/2 + 8k, ...) of the
+//     rotated part (eight rotation pairs), two consecutive chunks of the
+//     non-rotated tail, or of a V row -- loads it with two 16-byte loads, takes
+//     the row's sum of squares with shuffles among the row's lanes, rotates in
+//     registers and stores it with two 16-byte stores.  The only shared data
+//     are the cos/sin of the rd/2 pair indices, computed once per token.
+//   - rope_append_staged_kernel (any even rotary_dim): the rows are staged in
+//     shared memory and every thread works on independent (row, pair) slots.
 //
 // Precision.  The stored bf16 value is the correctly rounded result of the
-// exact rotation in all but vanishing cases, also where x0 cos - x1 sin nearly
-// cancels: the angle pos * inv_freq[i] is formed and reduced by whole turns in
-// double, its cos and sin come from double sincos (once per token and pair
-// index, shared by all heads) and are split into fp32 hi + lo parts; the
-// rotation is evaluated with error-free fp32 products (fmaf residuals) and an
-// error-free sum, so its absolute error is ~2^-44 of the operands.  The norm
-// weight enters as the exact product x * w of two bf16 values (for the
-// zero-centred style, x + x * w is kept as an fp32 hi + lo pair), and the row
-// factors (1 / rms, and the attention factor on the rotated dims) are applied
-// last as one relative rounding.
+// exact rotation, or one ulp off it only where the rotated value is below
+// ~2^-35 of its inputs:
+//   - The angle is taken in turns: pos * inv_freq / (2 pi) is formed exactly
+//     modulo 1 in 64-bit fixed point (inv_freq / (2 pi) is passed as a 96-bit
+//     fixed-point fraction, from a double-double division on the host; the
+//     product needs only integer multiplies).  Its top 8 bits select cos and sin
+//     of a multiple of 2 pi / 256 from a table built at compile time; the rest,
+//     |r| <= pi / 256, goes through the Taylor series of cos and sin evaluated
+//     in fp32 pairs (hi + lo, fmaf residuals for the leading products), and the
+//     two are combined with the angle-sum formulas.  Absolute error of cos and
+//     sin below 2^-43 (the rounding of the ~3e-7 low parts).
+//   - The rotation is evaluated with error-free fp32 products (fmaf residuals)
+//     and an error-free sum; the norm weight enters as the exact product x * w
+//     of two bf16 values (for the zero-centred style, x + x * w is kept as an
+//     fp32 hi + lo pair); the row factors (1 / rms, and the attention factor on
+//     the rotated dims) are applied last as one relative rounding.
 #include "na_internal.cuh"
 
 namespace {
 
-struct RopeTable {
-    double inv_freq[64];  // rd / 2 <= 64 (head_dim <= 128)
+// inv_freq[i] / (2 pi) in turns per position, as the 96-bit fixed-point
+// fraction hi * 2^-64 + lo * 2^-96.
+struct RopeTurns {
+    unsigned long long hi[64];  // rd / 2 <= 64 (head_dim <= 128)
+    unsigned int lo[64];
 };
 
-constexpr int kThreads = 256;
-constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr int kStagedThreads = 256;
+
+// pi as an unevaluated sum of two doubles (the high part is pi rounded to
+// double, the low part the next 53 bits).
+constexpr double kPiHi = 3.141592653589793116;
+constexpr double kPiLo = 1.2246467991473532e-16;
+constexpr double kStep = kPiHi / 128.0;  // 2 pi / 256
+
+// ------------------------------------------------- compile-time table --
+
+// Taylor series about 0, used by the table builder for |x| <= pi / 4 where
+// the terms fall below 1e-30 long before the loop ends.
+constexpr double series_sin(double x)
+{
+    double term = x, sum = x;
+    for (int n = 1; n < 20; ++n) {
+        term *= -x * x / ((2.0 * n) * (2.0 * n + 1.0));
+        sum += term;
+    }
+    return sum;
+}
+
+constexpr double series_cos(double x)
+{
+    double term = 1.0, sum = 1.0;
+    for (int n = 1; n < 20; ++n) {
+        term *= -x * x / ((2.0 * n - 1.0) * (2.0 * n));
+        sum += term;
+    }
+    return sum;
+}
+
+struct alignas(16) TrigEntry {
+    float ch, cl, sh, sl;  // cos and sin of 2 pi j / 256 as fp32 hi + lo pairs
+};
+struct TrigTable {
+    TrigEntry e[256];
+};
+
+// cos and sin of 2 pi j / 256: the angle is written as a quarter turn q plus
+// an offset within +-pi/4, whose series is evaluated; the quarter turn is
+// applied by exact swaps and sign changes.
+constexpr TrigTable make_trig_table()
+{
+    TrigTable t{};
+    for (int j = 0; j < 256; ++j) {
+        const int q = ((j + 32) / 64) % 4;
+        const int off = j - 64 * ((j + 32) / 64);  // in [-32, 32)
+        const double x = off * kStep;
+        const double c0 = series_cos(x), s0 = series_sin(x);
+        double c = c0, s = s0;
+        if (q == 1) {
+            c = -s0;
+            s = c0;
+        } else if (q == 2) {
+            c = -c0;
+            s = -s0;
+        } else if (q == 3) {
+            c = s0;
+            s = -c0;
+        }
+        const float ch = (float)c, sh = (float)s;
+        t.e[j] = TrigEntry{ch, (float)(c - (double)ch), sh, (float)(s - (double)sh)};
+    }
+    return t;
+}
+
+__device__ const TrigTable kTrig = make_trig_table();
+
+// 2 pi as an fp32 pair.
+constexpr float kTwoPiHi = (float)(2.0 * kPiHi);
+constexpr float kTwoPiLo = (float)((2.0 * kPiHi - (double)kTwoPiHi) + 2.0 * kPiLo);
+
+// ----------------------------------------------- fp32 pair arithmetic --
+
+struct F2 {
+    float hi, lo;  // unevaluated sum
+};
+
+// a * b + c * d of two pairs' products as a pair: leading products exact, their
+// sum error-free, cross terms rounded once.
+__host__ __device__ __forceinline__ F2 prod_sum(F2 a, F2 b, F2 c, F2 d)
+{
+    const float p0 = a.hi * b.hi;
+    const float e0 = fmaf(a.hi, b.hi, -p0);
+    const float p1 = c.hi * d.hi;
+    const float e1 = fmaf(c.hi, d.hi, -p1);
+    const float s = p0 + p1;
+    const float bb = s - p0;
+    const float t = (p0 - (s - bb)) + (p1 - bb);
+    const float cross = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, fmaf(c.hi, d.lo, c.lo * d.hi)));
+    return {s, t + (e0 + e1) + cross};
+}
+
+// cos and sin of 2 pi * pos * (fhi 2^-64 + flo 2^-96) as fp32 pairs
+// (cos hi, cos lo, sin hi, sin lo).
+__host__ __device__ __forceinline__ float4 cos_sin_turns(unsigned int pos, unsigned long long fhi,
+                                                         unsigned int flo, const TrigEntry *tab)
+{
+    // Fraction of a turn in units of 2^-64 (exact but for the dropped bits
+    // below 2^-64), rounded to the nearest 1/256 turn j plus a remainder.
+    unsigned long long u = (unsigned long long)pos * fhi + (((unsigned long long)pos * flo) >> 32);
+    u += 1ull << 55;
+    const int j = (int)(u >> 56);
+    const long long rem = (long long)(u & ((1ull << 56) - 1)) - (1ll << 55);  // |rem| <= 2^55
+    // rem * 2^-64 as an fp32 pair: three exactly representable pieces.
+    const int a_part = (int)(rem >> 32);  // |.| <= 2^23
+    const unsigned int b_part = (unsigned int)(rem & 0xffffffffll);
+    const float t1 = (float)a_part * 0x1p-32f;
+    const float t2 = (float)(b_part >> 8) * 0x1p-56f;
+    const float t3 = (float)(b_part & 255u) * 0x1p-64f;
+    const float rh0 = t1 + t2;
+    const float bb = rh0 - t1;
+    const float rl0 = ((t1 - (rh0 - bb)) + (t2 - bb)) + t3;
+    // r = 2 pi * remainder, radians, |r| <= pi / 256
+    const float dh = rh0 * kTwoPiHi;
+    const float dl = fmaf(rh0, kTwoPiHi, -dh) + fmaf(rh0, kTwoPiLo, rl0 * kTwoPiHi);
+
+    // Series of the remainder.
+    const float z = dh * dh;
+    const float ze = fmaf(dh, dh, -z);
+    // sin r = dh - dh^3/6 + dh^5/120 + dl (1 - dh^2/2)
+    const float p3 = dh * z;
+    const float p3e = fmaf(dh, z, -p3) + dh * ze;
+    const float sin_lo = dl * fmaf(z, -0.5f, 1.0f) - (p3 * (1.0f / 6.0f) + p3e * (1.0f / 6.0f)) +
+                         p3 * z * (1.0f / 120.0f);
+    const F2 sn = {dh, sin_lo};
+    // cos r = 1 - r^2/2 + r^4/24 - r^6/720, with r^2 = z + ze + 2 dh dl
+    const float half_z = 0.5f * z;
+    const float c0 = 1.0f - half_z;
+    const float c0e = (1.0f - c0) - half_z;
+    const float z2 = z * z;
+    const float cos_lo = c0e - 0.5f * ze - dh * dl + z2 * (1.0f / 24.0f) - z2 * z * (1.0f / 720.0f);
+    const F2 cs = {c0, cos_lo};
+
+    const TrigEntry e = tab[j];
+    const F2 tc = {e.ch, e.cl}, ts = {e.sh, e.sl};
+    const F2 nts = {-e.sh, -e.sl};
+    const F2 c = prod_sum(tc, cs, nts, sn);  // cos(t + r) = cos t cos r - sin t sin r
+    const F2 s = prod_sum(ts, cs, tc, sn);   // sin(t + r) = sin t cos r + cos t sin r
+    return make_float4(c.hi, c.lo, s.hi, s.lo);
+}
 
 // a = x * w as an unevaluated fp32 sum hi + lo (exact).
-struct F2 {
-    float hi, lo;
-};
-
 __device__ __forceinline__ F2 weighted(float x, float w, bool zero_centered)
 {
     const float p = x * w;
@@ -55,136 +208,314 @@ __device__ __forceinline__ F2 weighted(float x, float w, bool zero_centered)
     return {s, se + pe};
 }
 
-// u * c + v * d with u, v as hi + lo pairs and c, d as hi + lo pairs, returned
-// as hi + lo.  Leading products are exact (fmaf residuals); the leading sum is
-// error-free; the cross terms are small and rounded once.
-__device__ __forceinline__ F2 dot2(F2 u, float ch, float cl, F2 v, float dh, float dl)
+// Rotated pair (y0, y1) = (a0 cos - a1 sin, a0 sin + a1 cos) * fr.
+__device__ __forceinline__ void rotate(F2 a0, F2 a1, float4 c, float fr, float &y0, float &y1)
 {
-    const float p0 = u.hi * ch;
-    const float e0 = fmaf(u.hi, ch, -p0);
-    const float p1 = v.hi * dh;
-    const float e1 = fmaf(v.hi, dh, -p1);
-    const float s = p0 + p1;
-    const float bb = s - p0;
-    const float t = (p0 - (s - bb)) + (p1 - bb);
-    const float cross = fmaf(u.hi, cl, fmaf(u.lo, ch, fmaf(v.hi, dl, v.lo * dh)));
-    return {s, t + (e0 + e1) + cross};
+    const F2 r0 = prod_sum(a0, F2{c.x, c.y}, F2{-a1.hi, -a1.lo}, F2{c.z, c.w});
+    const F2 r1 = prod_sum(a0, F2{c.z, c.w}, a1, F2{c.x, c.y});
+    y0 = fmaf(r0.hi, fr, r0.lo * fr);
+    y1 = fmaf(r1.hi, fr, r1.lo * fr);
 }
 
-__global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendParams p,
-                                                               const RopeTable tab)
+__device__ __forceinline__ const bf16 *row_src(const RopeAppendParams &p, int t, int r)
 {
-    extern __shared__ float smem_f[];
-    const int t = blockIdx.x;
-    const int H = p.H, KV = p.KV, d = p.d, rows = H + 2 * KV;
-    const int half = p.rd / 2;
+    if (r < p.H)
+        return p.q + ((size_t)t * p.H + r) * p.d;
+    if (r < p.H + p.KV)
+        return p.k + ((size_t)t * p.KV + (r - p.H)) * p.d;
+    return p.v + ((size_t)t * p.KV + (r - p.H - p.KV)) * p.d;
+}
 
-    // Owner sequence: the last b with cu_seqlens[b] <= t (empty sequences skipped).
-    int lo = 0, hi = p.batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.cu_seqlens + mid) <= t)
-            lo = mid;
-        else
-            hi = mid - 1;
+__device__ __forceinline__ bf16 *row_dst(const RopeAppendParams &p, int t, int r, int b, int pos)
+{
+    const size_t cap = (size_t)p.capacity;
+    if (r < p.H)
+        return p.q_out + ((size_t)t * p.H + r) * p.d;
+    if (r < p.H + p.KV)
+        return p.cache_k + (((size_t)b * p.KV + (r - p.H)) * cap + pos) * p.d;
+    return p.cache_v + (((size_t)b * p.KV + (r - p.H - p.KV)) * cap + pos) * p.d;
+}
+
+// Owner sequence b of token t (the last b with cu_seqlens[b] <= t, empty
+// sequences skipped) and the token's position, a warp at a time: cu_seqlens
+// and cache_lens are read in the same round.
+__device__ __forceinline__ void owner_of(const RopeAppendParams &p, int t, int lane, int &b,
+                                         int &pos)
+{
+    b = 0;
+    pos = -1;
+    for (int base = 0; base < p.batch; base += 32) {
+        const int i = base + lane;
+        int cu = 0x7fffffff, cl = 0;
+        if (i < p.batch) {
+            cu = __ldg(p.cu_seqlens + i);
+            cl = __ldg(p.cache_lens + i);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, cu <= t);
+        if (m) {
+            const int src = 31 - __clz(m);
+            b = base + src;
+            pos = __shfl_sync(0xffffffffu, cl, src) + (t - __shfl_sync(0xffffffffu, cu, src));
+        }
+        if (m != 0xffffffffu)
+            break;
     }
-    const int b = lo;
-    const int pos = __ldg(p.cache_lens + b) + (t - __ldg(p.cu_seqlens + b));
+}
+
+// ------------------------------------------------------ register path --
+
+constexpr int kMaxUnits = 768;  // one unit per thread: up to 96 rows of d = 128
+
+template <int D>
+__global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppendParams p,
+                                                           const RopeTurns turns)
+{
+    constexpr int UPR = D / 16;  // 32-byte units per row
+    __shared__ TrigEntry trig[256];
+    __shared__ float4 cs[64];
+    const int t = blockIdx.x;
+    const int H = p.H, KV = p.KV, rows = H + 2 * KV;
+    const int half = p.rd / 2;
+    const int lane = threadIdx.x & 31;
+    const bool qk_norm = (p.flags & NA_QK_NORM) != 0;
+    const bool zero_centered = (p.flags & NA_QK_NORM_ZERO_CENTERED) != 0;
+    const bool v_norm = (p.flags & NA_V_NORM) != 0;
+
+    // This thread's unit: row r, 8-element chunks starting at e0 and e1.
+    const int unit = threadIdx.x;
+    const bool active = unit < rows * UPR;
+    const int r = unit / UPR, k = unit % UPR;
+    const bool is_v = r >= H + KV;
+    const bool rot = !is_v && k < p.rd / 16;
+    int e0, e1;
+    if (is_v) {
+        e0 = 16 * k;
+        e1 = e0 + 8;
+    } else if (rot) {
+        e0 = 8 * k;
+        e1 = half + 8 * k;
+    } else {
+        e0 = p.rd + 16 * (k - p.rd / 16);
+        e1 = e0 + 8;
+    }
+
+    // Everything the token needs is requested first.
+    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, wa = xa, wb = xa;
+    if (active) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(row_src(p, t, r));
+        xa = __ldg(src + e0 / 8);
+        xb = __ldg(src + e1 / 8);
+        if (qk_norm && !is_v) {
+            const uint4 *w = reinterpret_cast<const uint4 *>(r < H ? p.qw : p.kw);
+            wa = __ldg(w + e0 / 8);
+            wb = __ldg(w + e1 / 8);
+        }
+    }
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+        reinterpret_cast<uint4 *>(trig)[i] = __ldg(reinterpret_cast<const uint4 *>(&kTrig) + i);
+    int b, pos;
+    owner_of(p, t, lane, b, pos);
     if (pos < 0 || pos >= p.capacity) {
         if (threadIdx.x == 0)
             na_report(p.status, NA_ERR_CAPACITY);
         return;
     }
+    __syncthreads();
+    if ((int)threadIdx.x < half)
+        cs[threadIdx.x] = cos_sin_turns((unsigned)pos, turns.hi[threadIdx.x], turns.lo[threadIdx.x],
+                                        trig);
+    __syncthreads();
+
+    float a[8], c[8];
+    bf16x8_to_f32(xa, a);
+    bf16x8_to_f32(xb, c);
+    const bool normed = is_v ? v_norm : qk_norm;
+    float f = 1.0f;
+    if (qk_norm || v_norm) {  // every lane shuffles; rows are aligned to UPR lanes
+        float ss = 0.f;      // squares of bf16 values are exact in fp32
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            ss = fmaf(a[i], a[i], fmaf(c[i], c[i], ss));
+#pragma unroll
+        for (int o = UPR / 2; o; o >>= 1)
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (normed)
+            f = 1.0f / sqrtf(ss / (float)D + p.eps);
+    }
+    if (!active)
+        return;
+
+    float ya[8], yb[8];
+    if (is_v) {
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            ya[i] = a[i] * f;
+            yb[i] = c[i] * f;
+        }
+    } else {
+        F2 xa2[8], xb2[8];
+        if (qk_norm) {
+            float wfa[8], wfb[8];
+            bf16x8_to_f32(wa, wfa);
+            bf16x8_to_f32(wb, wfb);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                xa2[i] = weighted(a[i], wfa[i], zero_centered);
+                xb2[i] = weighted(c[i], wfb[i], zero_centered);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                xa2[i] = F2{a[i], 0.f};
+                xb2[i] = F2{c[i], 0.f};
+            }
+        }
+        if (rot) {
+            const float fr = f * p.rope_scale;  // the attention factor scales rotated dims only
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                rotate(xa2[i], xb2[i], cs[8 * k + i], fr, ya[i], yb[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                ya[i] = fmaf(xa2[i].hi, f, xa2[i].lo * f);
+                yb[i] = fmaf(xb2[i].hi, f, xb2[i].lo * f);
+            }
+        }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(row_dst(p, t, r, b, pos));
+    dst[e0 / 8] = f32_to_bf16x8(ya);
+    dst[e1 / 8] = f32_to_bf16x8(yb);
+}
+
+// -------------------------------------------------------- staged path --
+
+__global__ void __launch_bounds__(kStagedThreads) rope_append_staged_kernel(const RopeAppendParams p,
+                                                                           const RopeTurns turns)
+{
+    extern __shared__ float smem_f[];
+    const int t = blockIdx.x;
+    const int H = p.H, KV = p.KV, d = p.d, rows = H + 2 * KV;
+    const int half = p.rd / 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool qk_norm = (p.flags & NA_QK_NORM) != 0;
+    const bool zero_centered = (p.flags & NA_QK_NORM_ZERO_CENTERED) != 0;
+    const bool v_norm = (p.flags & NA_V_NORM) != 0;
 
     float *xs = smem_f;                                          // [rows][d]
-    float4 *cs = reinterpret_cast<float4 *>(smem_f + rows * d);  // [half] (cos hi, cos lo, sin hi, sin lo)
-
-    for (int i = threadIdx.x; i < half; i += kThreads) {
-        const double angle = (double)pos * tab.inv_freq[i];
-        const double r = fma(-rint(angle * (1.0 / kTwoPi)), kTwoPi, angle);
-        double sd, cd;
-        sincos(r, &sd, &cd);
-        const float ch = (float)cd, sh = (float)sd;
-        cs[i] = make_float4(ch, (float)(cd - (double)ch), sh, (float)(sd - (double)sh));
-    }
+    float4 *cs = reinterpret_cast<float4 *>(xs + rows * d);      // [64] (cos hi, lo, sin hi, lo)
+    TrigEntry *trig = reinterpret_cast<TrigEntry *>(cs + 64);    // [256]
+    float *wq = reinterpret_cast<float *>(trig + 256);           // [d] q norm weights
+    float *wk = wq + d;                                          // [d] k norm weights
+    float *rf = wk + d;                                          // [rows] 1 / rms per row
 
     const int cpr = d / 8;  // 16-byte chunks per row
-    for (int c = threadIdx.x; c < rows * cpr; c += kThreads) {
-        const int r = c / cpr, j = c - r * cpr;
-        const bf16 *src;
-        if (r < H)
-            src = p.q + ((size_t)t * H + r) * d;
-        else if (r < H + KV)
-            src = p.k + ((size_t)t * KV + (r - H)) * d;
-        else
-            src = p.v + ((size_t)t * KV + (r - H - KV)) * d;
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src) + j);
+    const int chunks = rows * cpr;
+    for (int i = threadIdx.x; i < 256; i += kStagedThreads)
+        reinterpret_cast<uint4 *>(trig)[i] = __ldg(reinterpret_cast<const uint4 *>(&kTrig) + i);
+    int b, pos;
+    owner_of(p, t, lane, b, pos);
+    if (pos < 0 || pos >= p.capacity) {
+        if (threadIdx.x == 0)
+            na_report(p.status, NA_ERR_CAPACITY);
+        return;
+    }
+    if (qk_norm) {
+        for (int i = threadIdx.x; i < 2 * d; i += kStagedThreads)
+            wq[i] = __bfloat162float(i < d ? p.qw[i] : p.kw[i - d]);
+    }
+    for (int c = threadIdx.x; c < chunks; c += kStagedThreads) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(row_src(p, t, c / cpr)) + (c % cpr));
         float f[8];
         bf16x8_to_f32(u, f);
-        float4 *dst = reinterpret_cast<float4 *>(xs + r * d + j * 8);
+        float4 *dst = reinterpret_cast<float4 *>(xs + c * 8);
         dst[0] = make_float4(f[0], f[1], f[2], f[3]);
         dst[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
     __syncthreads();
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool qk_norm = (p.flags & NA_QK_NORM) != 0;
-    const bool zero_centered = (p.flags & NA_QK_NORM_ZERO_CENTERED) != 0;
-    const bool v_norm = (p.flags & NA_V_NORM) != 0;
-    for (int r = warp; r < rows; r += kThreads / 32) {
-        float *x = xs + r * d;
-        const bool is_v = r >= H + KV;
-        const bool normed = is_v ? v_norm : qk_norm;
-        float f = 1.0f;  // row factor (1 / rms), applied last
-        if (normed) {
-            float ss = 0.f;  // squares of bf16 values are exact in fp32
-            for (int i = lane; i < d; i += 32)
-                ss = fmaf(x[i], x[i], ss);
+    // cos/sin per pair index (two warps) while the other warps take row norms.
+    if (threadIdx.x < 64) {
+        if ((int)threadIdx.x < half)
+            cs[threadIdx.x] = cos_sin_turns((unsigned)pos, turns.hi[threadIdx.x],
+                                            turns.lo[threadIdx.x], trig);
+    } else if (qk_norm || v_norm) {
+        for (int r = warp - 2; r < rows; r += kStagedThreads / 32 - 2) {
+            const bool is_v = r >= H + KV;
+            float f = 1.0f;
+            if (is_v ? v_norm : qk_norm) {
+                const float *x = xs + r * d;
+                float ss = 0.f;
+                for (int i = lane; i < d; i += 32)
+                    ss = fmaf(x[i], x[i], ss);
 #pragma unroll
-            for (int o = 16; o; o >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            f = 1.0f / sqrtf(ss / (float)d + p.eps);
-        }
-        if (is_v) {
-            for (int i = lane; i < d; i += 32)
-                x[i] *= f;
-            continue;
-        }
-        const bf16 *wp = normed ? (r < H ? p.qw : p.kw) : nullptr;
-        auto a_of = [&](int i) -> F2 {
-            if (!wp)
-                return {x[i], 0.f};
-            return weighted(x[i], __bfloat162float(wp[i]), zero_centered);
-        };
-        const float fr = f * p.rope_scale;  // the attention factor scales rotated dims only
-        for (int i = lane; i < half; i += 32) {
-            const float4 c = cs[i];
-            const F2 a0 = a_of(i), a1 = a_of(i + half);
-            const F2 neg_a1 = {-a1.hi, -a1.lo};
-            const F2 y0 = dot2(a0, c.x, c.y, neg_a1, c.z, c.w);  // a0 cos - a1 sin
-            const F2 y1 = dot2(a0, c.z, c.w, a1, c.x, c.y);      // a0 sin + a1 cos
-            x[i] = fmaf(y0.hi, fr, y0.lo * fr);
-            x[i + half] = fmaf(y1.hi, fr, y1.lo * fr);
-        }
-        for (int i = p.rd + lane; i < d; i += 32) {
-            const F2 a = a_of(i);
-            x[i] = fmaf(a.hi, f, a.lo * f);
+                for (int o = 16; o; o >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                f = 1.0f / sqrtf(ss / (float)d + p.eps);
+            }
+            if (lane == 0)
+                rf[r] = f;
         }
     }
     __syncthreads();
 
-    const size_t cap = (size_t)p.capacity;
-    for (int c = threadIdx.x; c < rows * cpr; c += kThreads) {
-        const int r = c / cpr, j = c - r * cpr;
-        bf16 *dst;
-        if (r < H)
-            dst = p.q_out + ((size_t)t * H + r) * d;
-        else if (r < H + KV)
-            dst = p.cache_k + (((size_t)b * KV + (r - H)) * cap + pos) * d;
-        else
-            dst = p.cache_v + (((size_t)b * KV + (r - H - KV)) * cap + pos) * d;
-        reinterpret_cast<uint4 *>(dst)[j] = f32_to_bf16x8(xs + r * d + j * 8);
+    // Every row has d/2 slots.  Q and K rows: slot i < half is the pair
+    // (i, i + half), the rest cover the non-rotated tail two elements at a
+    // time; V rows: elements (2i, 2i + 1).
+    const int slots = d / 2;
+    const int items = rows * slots;
+    const bool any_norm = qk_norm || v_norm;
+    for (int it = threadIdx.x; it < items; it += kStagedThreads) {
+        const int r = it / slots, i = it - r * slots;
+        float *x = xs + r * d;
+        const float f = any_norm ? rf[r] : 1.0f;
+        if (r >= H + KV) {
+            if (v_norm) {
+                x[2 * i] *= f;
+                x[2 * i + 1] *= f;
+            }
+            continue;
+        }
+        const float *w = qk_norm ? (r < H ? wq : wk) : nullptr;
+        auto a_of = [&](int e) -> F2 {
+            if (!w)
+                return {x[e], 0.f};
+            return weighted(x[e], w[e], zero_centered);
+        };
+        if (i < half) {
+            float y0, y1;
+            rotate(a_of(i), a_of(i + half), cs[i], f * p.rope_scale, y0, y1);
+            x[i] = y0;
+            x[i + half] = y1;
+        } else {
+            const int e0 = p.rd + 2 * (i - half);
+            const F2 a0 = a_of(e0), a1 = a_of(e0 + 1);
+            x[e0] = fmaf(a0.hi, f, a0.lo * f);
+            x[e0 + 1] = fmaf(a1.hi, f, a1.lo * f);
+        }
     }
+    __syncthreads();
+
+    for (int c = threadIdx.x; c < chunks; c += kStagedThreads) {
+        const int r = c / cpr, j = c - r * cpr;
+        reinterpret_cast<uint4 *>(row_dst(p, t, r, b, pos))[j] = f32_to_bf16x8(xs + r * d + j * 8);
+    }
+}
+
+// inv_freq / (2 pi) as a 96-bit fixed-point fraction.  The quotient is formed
+// as a double-double (error ~2^-104 relative), then each part is converted to
+// fixed point exactly.
+void turns_fixed_point(double inv_freq, unsigned long long &hi, unsigned int &lo)
+{
+    const double bh = 2.0 * kPiHi, bl = 2.0 * kPiLo;
+    const double q1 = inv_freq / bh;
+    const double p = q1 * bh;
+    const double pe = fma(q1, bh, -p);
+    const double rsd = ((inv_freq - p) - pe) - q1 * bl;
+    const double q2 = rsd / bh;
+    const __int128 x = (__int128)ldexp(q1, 96) + (__int128)nearbyint(ldexp(q2, 96));
+    hi = (unsigned long long)(x >> 32);
+    lo = (unsigned int)(x & 0xffffffff);
 }
 
 }  // namespace
@@ -192,24 +523,37 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendP
 cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq, int half,
                                cudaStream_t stream)
 {
-    RopeTable tab;
-    for (int i = 0; i < 64; i++)
-        tab.inv_freq[i] = i < half ? inv_freq[i] : 0.0;
+    RopeTurns turns{};
+    for (int i = 0; i < half && i < 64; i++)
+        turns_fixed_point(inv_freq[i], turns.hi[i], turns.lo[i]);
+    const int units = (p.H + 2 * p.KV) * (p.d / 16);
+    if (p.rd % 16 == 0 && units <= kMaxUnits) {
+        int threads = (units + 31) / 32 * 32;
+        if (threads < 64)
+            threads = 64;
+        if (p.d == 128)
+            rope_append_kernel<128><<<p.total_tokens, threads, 0, stream>>>(p, turns);
+        else
+            rope_append_kernel<64><<<p.total_tokens, threads, 0, stream>>>(p, turns);
+        return cudaGetLastError();
+    }
     const size_t smem = rope_append_smem_bytes(p.H, p.KV, p.d, p.rd);
     static size_t configured = 0;
     if (smem > 48 * 1024 && smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(rope_append_kernel,
+        cudaError_t e = cudaFuncSetAttribute(rope_append_staged_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess)
             return e;
         configured = smem;
     }
-    rope_append_kernel<<<p.total_tokens, kThreads, smem, stream>>>(p, tab);
+    rope_append_staged_kernel<<<p.total_tokens, kStagedThreads, smem, stream>>>(p, turns);
     return cudaGetLastError();
 }
 
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd)
 {
-    return ((size_t)(H + 2 * KV) * d + 4 * (size_t)(rd / 2)) * sizeof(float);
+    (void)rd;
+    const size_t rows = (size_t)(H + 2 * KV);
+    return (rows * d + 64 * 4 + 256 * 4 + 2 * (size_t)d + rows) * sizeof(float);
 }

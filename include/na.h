@@ -105,7 +105,8 @@ typedef struct na_kv_cache {
  *   cache_lens    int32 [batch]: tokens already cached (prior length).
  *   total_tokens  HOST copy of cu_seqlens[batch]; 0 is a no-op returning NA_OK.
  *   q             bf16 [total_tokens][H][d];  k, v bf16 [total_tokens][KV][d].
- *   q_norm_w, k_norm_w  bf16 [d] (shared by all heads), required with NA_QK_NORM, else ignored.
+ *   q_norm_w, k_norm_w  bf16 [d] (shared by all heads), 16-byte aligned, required with
+ *              NA_QK_NORM, else ignored.
  *   q_out         bf16 [total_tokens][H][d]: rotated queries (may not alias q).
  *   status        device int32 or NULL; a token whose pos >= capacity is skipped and
  *                 NA_ERR_CAPACITY is written.

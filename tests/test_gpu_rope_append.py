@@ -25,6 +25,18 @@ CASES = {
                                                           orig_max_pos=8192, attn_factor=1.0)),
         [100], [33], 256),
     "no_rotary": (W.Spec(H=4, KV=4, d=128, rd=0), [2], [7], 16),
+    # rotary_dim not a multiple of 16, and more rows than one thread each: the
+    # shared-memory staged kernel
+    "staged_rd24_d64_qknorm_vnorm": (
+        W.Spec(H=4, KV=2, d=64, rd=24, rope=W.RopeParams(base=1e4), qk_norm=True, v_norm=True),
+        [40, 3], [6, 9], 64),
+    "staged_rd40_d128_yarn": (
+        W.Spec(H=8, KV=4, d=128, rd=40, rope=W.RopeParams(base=1e6, yarn=True, factor=4.0,
+                                                          orig_max_pos=8192)),
+        [9000], [12], 9100),
+    "staged_h96kv8_many_rows": (W.Spec(H=96, KV=8, d=128, rd=128), [0, 500], [5, 3], 512),
+    "register_h80kv8_widest": (W.Spec(H=80, KV=8, d=128, rd=128, qk_norm=True), [0, 70], [4, 2],
+                               128),
 }
 
 
