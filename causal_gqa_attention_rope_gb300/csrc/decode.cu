@@ -223,6 +223,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
         sm.abort_flag = 0;
         fence_barrier_init();
     }
+    grid_dependency_wait();
+    grid_dependents_launch();
     if (warp == DEC_CWARPS)
         locate_slice(p, lane, sm.slice);
     __syncthreads();
@@ -506,6 +508,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p)
 {
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int bh = blockIdx.x;
     const int b = bh / p.H;
     const int n = __ldg(p.kv_lens + b);
@@ -595,12 +599,11 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
             return e;
         configured = true;
     }
-    decode_split_kernel<D, HPC><<<p.grid, DEC_THREADS, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(decode_split_kernel<D, HPC>, dim3(p.grid), dim3(DEC_THREADS), smem,
+                                  stream, p);
     if (e != cudaSuccess)
         return e;
-    decode_combine_kernel<D><<<p.batch * p.H, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(decode_combine_kernel<D>, dim3(p.batch * p.H), dim3(256), 0, stream, p);
 }
 
 }  // namespace

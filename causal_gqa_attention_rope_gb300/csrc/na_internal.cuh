@@ -149,6 +149,46 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Every kernel of this library is launched with programmatic stream
+// serialization, so it may be scheduled while its predecessor in the stream is
+// still finishing.  Each kernel first does the part of its prologue that reads
+// no global memory (barrier set-up, tensor-memory allocation, descriptor
+// prefetch), then grid_dependency_wait() -- it returns once every prerequisite
+// grid has completed and its writes are visible, at once when there is none --
+// and then grid_dependents_launch(), after which the next kernel in the stream
+// may be scheduled.  A dependent grid is therefore only launched once all CTAs
+// of the current grid are resident and past their wait, so a waiting grid can
+// never hold the resources its predecessor needs to finish.
+constexpr bool kProgrammaticLaunch = true;
+
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ------------------------------------------------------ launch parameters --
 
 struct RopeAppendParams {

@@ -11,6 +11,8 @@
 // Warp roles (8 warps):
 //   warp 0     TMA producer: the Q tile once, then K and V tiles into a
 //              3-stage ring (128-byte swizzled, as the MMA descriptors expect);
+//              the Q tile and the first three stages are issued by the thread
+//              that initialises the barriers, before the CTA-wide barrier;
 //   warp 1     allocates tensor memory; one lane issues S_j = Q K_j^T (SS, both
 //              K-major) into one of three S buffers in tensor memory;
 //   warp 2     one lane issues O += P_j V_j (TS: P read from tensor memory over
@@ -24,7 +26,9 @@
 //              rescaled in tensor memory), exponentiate on the MUFU unit
 //              (measured faster than moving part of the exponentials to a
 //              polynomial on the FMA pipe), write P_j as bf16 over S_j, and
-//              finally normalise, gate and store O.
+//              finally normalise and gate O, staging it through the idle K ring
+//              so that each warp stores whole rows (coalesced) instead of one
+//              16-byte piece of 32 different rows per instruction.
 // With three S buffers the tensor core computes S_{j+1} and S_{j+2} while the
 // softmax works on tile j, and PV_j runs while it prepares P_{j+1}.
 //
@@ -99,40 +103,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     TcSmem<D> &sm = *reinterpret_cast<TcSmem<D> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    // ------------------------------------------------------------ the tile --
-    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const int h = blockIdx.y;
-    const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
-    const int tok0 = __ldg(p.cu_seqlens + b);
-    const int n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
-    const int r0 = qt * BM;
-    if (n_new > p.max_new_len) {
-        if (qt == 0 && h == 0 && threadIdx.x == 0)
-            na_report(p.status, NA_ERR_INVALID_ARG);
-        return;
-    }
-    if (r0 >= n_new)
-        return;
-    const int prior = __ldg(p.cache_lens + b);
-    const int rows = min(BM, n_new - r0);
-    const int pos_lo = prior + r0, pos_hi = prior + r0 + rows - 1;
-    if (prior < 0 || pos_hi >= p.capacity || pos_hi >= p.max_total_len) {
-        if (threadIdx.x == 0)
-            na_report(p.status, NA_ERR_CAPACITY);
-        return;
-    }
-    int k_begin = 0, k_end = pos_hi + 1;
-    if (p.num_splits > 1) {
-        k_begin = split * p.split_len;
-        k_end = min(k_end, k_begin + p.split_len);
-    }
-    if (k_begin >= k_end)
-        return;
-    const int n_tiles = (k_end - k_begin + BN - 1) / BN;
-    const int kvh = h / p.group;
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Prologue that reads no global memory: descriptor prefetch, barriers and
+    // tensor memory; it may overlap the end of the previous kernel.
     if (threadIdx.x == 0) {
+        tc::prefetch_tmap(&map_q);
+        tc::prefetch_tmap(&map_k);
+        tc::prefetch_tmap(&map_v);
         mbar_init(&sm.q_full, 1);
         for (int s = 0; s < STAGES; s++) {
             mbar_init(&sm.k_full[s], 1);
@@ -153,6 +130,94 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (warp == 1)
         tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    grid_dependency_wait();
+    grid_dependents_launch();
+
+    // ------------------------------------------------------------ the tile --
+    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
+    const int h = blockIdx.y;
+    const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
+    const int kvh = h / p.group;
+    const int r0 = qt * BM;
+    const int k_begin = p.num_splits > 1 ? split * p.split_len : 0;
+    const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
+    // The first K and V tiles depend only on the block, and the first
+    // sequence's tokens start at row 0: those copies are issued before the
+    // sequence bounds arrive, overlapping that round trip (a CTA that turns
+    // out to have no work waits for them before it exits).
+    const bool early_q = b == 0;
+    if (threadIdx.x == 0) {
+        if (early_q) {
+            mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
+            for (int kb = 0; kb < KB; kb++)
+                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, r0, &sm.q_full);
+        }
+        mbar_arrive_expect_tx(&sm.k_full[0], KB * BN * 128);
+        for (int kb = 0; kb < KB; kb++)
+            tc::tma_load_2d(sm.k[0][kb], &map_k, kb * 64, row_base, &sm.k_full[0]);
+        mbar_arrive_expect_tx(&sm.v_full[0], KB * BN * 128);
+        for (int kb = 0; kb < KB; kb++)
+            tc::tma_load_2d(sm.v[0][kb], &map_v, kb * 64, row_base, &sm.v_full[0]);
+    }
+    const int tok0 = __ldg(p.cu_seqlens + b);
+    const int n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
+    const int prior = __ldg(p.cache_lens + b);
+    const int rows = min(BM, n_new - r0);
+    const int pos_lo = prior + r0, pos_hi = prior + r0 + rows - 1;
+    int k_end = pos_hi + 1;
+    if (p.num_splits > 1)
+        k_end = min(k_end, k_begin + p.split_len);
+    bool run = true;  // uniform over the CTA
+    if (n_new > p.max_new_len || (b == 0 && tok0 != 0)) {
+        if (qt == 0 && h == 0 && split == 0 && threadIdx.x == 0)
+            na_report(p.status, NA_ERR_INVALID_ARG);
+        run = false;
+    } else if (r0 >= n_new) {
+        run = false;
+    } else if (prior < 0 || pos_hi >= p.capacity || pos_hi >= p.max_total_len) {
+        if (threadIdx.x == 0)
+            na_report(p.status, NA_ERR_CAPACITY);
+        run = false;
+    } else if (k_begin >= k_end) {
+        run = false;
+    }
+    if (!run) {  // nothing to attend: let the early copies land, give the tensor memory back
+        if (threadIdx.x == 0) {
+            if (early_q)
+                mbar_wait_bounded(&sm.q_full, 0);
+            mbar_wait_bounded(&sm.k_full[0], 0);
+            mbar_wait_bounded(&sm.v_full[0], 0);
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 1) {
+            tc::fence_after_sync();
+            tc::tmem_dealloc(sm.tmem_base, TMEM_COLS);
+        }
+        return;
+    }
+    const int n_tiles = (k_end - k_begin + BN - 1) / BN;
+    const int pre = n_tiles < STAGES ? n_tiles : STAGES;  // tiles loaded before the barrier
+
+    if (threadIdx.x == 0) {
+        // The Q tile (unless already issued) and the remaining first ring
+        // stages go out before the CTA-wide barrier (fresh stages need no
+        // wait), so these copies overlap the tensor-memory allocation and the
+        // barrier itself.
+        if (!early_q) {
+            mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
+            for (int kb = 0; kb < KB; kb++)
+                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, tok0 + r0, &sm.q_full);
+        }
+        for (int j = 1; j < pre; j++) {
+            mbar_arrive_expect_tx(&sm.k_full[j], KB * BN * 128);
+            for (int kb = 0; kb < KB; kb++)
+                tc::tma_load_2d(sm.k[j][kb], &map_k, kb * 64, row_base + j * BN, &sm.k_full[j]);
+            mbar_arrive_expect_tx(&sm.v_full[j], KB * BN * 128);
+            for (int kb = 0; kb < KB; kb++)
+                tc::tma_load_2d(sm.v[j][kb], &map_v, kb * 64, row_base + j * BN, &sm.v_full[j]);
+        }
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -161,15 +226,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
-            tc::prefetch_tmap(&map_q);
-            tc::prefetch_tmap(&map_k);
-            tc::prefetch_tmap(&map_v);
-            const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
-            mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
-            for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, tok0 + r0, &sm.q_full);
-            int issued = 0;
-            for (int j = 0; j < n_tiles; j++) {
+            int issued = pre;
+            for (int j = pre; j < n_tiles; j++) {
                 const int st = j % STAGES;
                 const uint32_t par = ((j / STAGES) & 1) ^ 1;
                 if (!mbar_wait_bounded(&sm.k_empty[st], par) || aborted(&sm.abort_flag)) {
@@ -392,60 +450,81 @@ __global__ void __launch_bounds__(THREADS, 1)
                 set_abort(&sm.abort_flag, p.status);
         } else if (mbar_wait_bounded(&sm.o_done, (n_tiles - 1) & 1)) {
             // ---------------------------------------------------- epilogue --
+            // Each thread writes its O row (normalised unless this is a split
+            // partial) into the idle K ring, rows padded by 16 bytes so the
+            // row-per-thread writes are bank-conflict free; then each warp
+            // stores its 32 rows one row per instruction, coalesced.
             tc::fence_after_sync();
-            const size_t tok = (size_t)(tok0 + r0 + r);
-            const bool valid = r < rows;
-            if (p.num_splits == 1) {
-                const float inv = l > 0.f ? 1.0f / l : 0.f;
-                bf16 *dst = p.out + (tok * p.H + h) * D;
-                const bool gated = (p.flags & NA_OUT_GATE) && p.gate;
+            constexpr int LDS = D + 4;
+            constexpr int EPL = D / 32;  // elements per lane in the row stores
+            float *stage = reinterpret_cast<float *>(&sm.k[0][0][0]);
+            const bool split_out = p.num_splits > 1;
+            const float scale = split_out ? 1.0f : (l > 0.f ? 1.0f / l : 0.f);
+            {
+                uint32_t o[D / 32][32];  // the whole row in one round of loads
+#pragma unroll
+                for (int c = 0; c < D / 32; c++)
+                    tc::tmem_ld32(o_t + c * 32, o[c]);
+                tc::tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < D / 32; c++) {
-                    uint32_t o[32];
-                    tc::tmem_ld32(o_t + c * 32, o);
-                    tc::tmem_wait_ld();
-                    if (!valid)
-                        continue;
-                    float f[32];
-#pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        f[i] = __uint_as_float(o[i]) * inv;
-                    if (gated) {
-                        const uint4 *g4 =
-                            reinterpret_cast<const uint4 *>(p.gate + (tok * p.H + h) * D + c * 32);
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            float g[8];
-                            bf16x8_to_f32(__ldg(g4 + q), g);
-#pragma unroll
-                            for (int e = 0; e < 8; e++)
-                                f[q * 8 + e] *= 1.0f / (1.0f + __expf(-g[e]));
-                        }
-                    }
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        d4[q] = f32_to_bf16x8(f + q * 8);
-                }
-            } else {
-                const size_t row = (tok * p.H + h) * p.num_splits + split;
-                float *dst = p.part_o + row * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; c++) {
-                    uint32_t o[32];
-                    tc::tmem_ld32(o_t + c * 32, o);
-                    tc::tmem_wait_ld();
-                    if (!valid)
-                        continue;
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+                    float4 *row4 = reinterpret_cast<float4 *>(stage + r * LDS + c * 32);
 #pragma unroll
                     for (int q = 0; q < 8; q++)
-                        d4[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                            __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+                        row4[q] = make_float4(__uint_as_float(o[c][4 * q]) * scale,
+                                              __uint_as_float(o[c][4 * q + 1]) * scale,
+                                              __uint_as_float(o[c][4 * q + 2]) * scale,
+                                              __uint_as_float(o[c][4 * q + 3]) * scale);
                 }
-                if (valid) {
-                    p.part_ml[row * 2] = m_ref;
-                    p.part_ml[row * 2 + 1] = l;
+            }
+            if (split_out && r < rows) {
+                const size_t row = ((size_t)(tok0 + r0 + r) * p.H + h) * p.num_splits + split;
+                p.part_ml[row * 2] = m_ref;
+                p.part_ml[row * 2 + 1] = l;
+            }
+            __syncwarp();
+            const bool gated = !split_out && (p.flags & NA_OUT_GATE) && p.gate;
+#pragma unroll 8
+            for (int i = 0; i < 32; i++) {
+                const int rr = quarter * 32 + i;
+                if (rr >= rows)
+                    break;
+                const size_t tok = (size_t)(tok0 + r0 + rr);
+                const float *src = stage + rr * LDS + lane * EPL;
+                float v[EPL];
+                if constexpr (EPL == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src);
+                    v[0] = x.x;
+                    v[1] = x.y;
+                    v[2] = x.z;
+                    v[3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(src);
+                    v[0] = x.x;
+                    v[1] = x.y;
+                }
+                if (split_out) {
+                    float *dst = p.part_o + ((tok * p.H + h) * p.num_splits + split) * D + lane * EPL;
+                    if constexpr (EPL == 4)
+                        *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                    else
+                        *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+                } else {
+                    const size_t off = (tok * p.H + h) * D + lane * EPL;
+                    if (gated) {
+                        const bf16 *g = p.gate + off;
+#pragma unroll
+                        for (int e = 0; e < EPL; e++)
+                            v[e] *= 1.0f / (1.0f + __expf(-__bfloat162float(g[e])));
+                    }
+                    uint32_t pk[EPL / 2];
+#pragma unroll
+                    for (int e = 0; e < EPL; e += 2)
+                        pk[e / 2] = pack_bf16x2(v[e], v[e + 1]);
+                    if constexpr (EPL == 4)
+                        *reinterpret_cast<uint2 *>(p.out + off) = make_uint2(pk[0], pk[1]);
+                    else
+                        *reinterpret_cast<uint32_t *>(p.out + off) = pk[0];
                 }
             }
         } else if (lane == 0) {
@@ -461,60 +540,128 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// Merge the KV splits of each (token, head) row: one warp per row.
+// Merge the KV splits of each (token, head) row: one warp per row.  The
+// owner sequence and every split's (max, sum) are read in one round (lane s
+// holds split s), then each lane reads its D/32 output elements of every split
+// with all the loads in flight at once.
 template <int D>
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParams p, int total_tokens)
 {
+    constexpr int EPL = D / 32;  // output elements per lane
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    const unsigned FULL = 0xffffffffu;
     if (row >= total_tokens * p.H)
         return;
     const int t = row / p.H;
-    int lo = 0, hi = p.batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.cu_seqlens + mid) <= t)
-            lo = mid;
-        else
-            hi = mid - 1;
+    const float *ml = p.part_ml + (size_t)row * p.num_splits * 2;
+    const float2 ml0 = lane < p.num_splits ? *reinterpret_cast<const float2 *>(ml + 2 * lane)
+                                           : make_float2(-INFINITY, 0.f);
+    // Owner sequence: the last b with cu_seqlens[b] <= t, a warp at a time.
+    int b = 0, pos = -1;
+    for (int base = 0; base < p.batch; base += 32) {
+        const int i = base + lane;
+        int cu = 0x7fffffff, cl = 0;
+        if (i < p.batch) {
+            cu = __ldg(p.cu_seqlens + i);
+            cl = __ldg(p.cache_lens + i);
+        }
+        const unsigned m = __ballot_sync(FULL, cu <= t);
+        if (m) {
+            const int src = 31 - __clz(m);
+            b = base + src;
+            pos = __shfl_sync(FULL, cl, src) + (t - __shfl_sync(FULL, cu, src));
+        }
+        if (m != FULL)
+            break;
     }
-    const int pos = __ldg(p.cache_lens + lo) + (t - __ldg(p.cu_seqlens + lo));
     if (pos < 0 || pos >= p.capacity || pos >= p.max_total_len)
         return;  // reported by the split pass
     const int ns = min(p.num_splits, pos / p.split_len + 1);
-    const float *ml = p.part_ml + (size_t)row * p.num_splits * 2;
+
+    // Global maximum and sum over the splits this row has keys in.
     float M = -INFINITY;
-    for (int s = 0; s < ns; s++)
-        M = fmaxf(M, ml[2 * s]);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        const float m = s0 + lane < ns ? (s0 == 0 ? ml0.x : ml[2 * (s0 + lane)]) : -INFINITY;
+        M = fmaxf(M, m);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+
+    const float *po = p.part_o + (size_t)row * p.num_splits * D + lane * EPL;
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; e++)
+        acc[e] = 0.f;
     float L = 0.f;
-    float w[16];
-    for (int s = 0; s < ns && s < 16; s++) {
-        w[s] = exp2f(ml[2 * s] - M);
-        L += ml[2 * s + 1] * w[s];
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        float w = 0.f;  // this lane's split weight 2^(m - M)
+        if (s0 + lane < ns) {
+            const float2 v = s0 == 0 ? ml0 : *reinterpret_cast<const float2 *>(ml + 2 * (s0 + lane));
+            w = exp2f(v.x - M);
+            L = fmaf(v.y, w, L);
+        }
+        const int n = min(32, ns - s0);
+        int s = 0;
+        for (; s + 4 <= n; s += 4) {
+            float v[4][EPL];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const float *src = po + (size_t)(s0 + s + u) * D;
+                if constexpr (EPL == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src);
+                    v[u][0] = x.x;
+                    v[u][1] = x.y;
+                    v[u][2] = x.z;
+                    v[u][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(src);
+                    v[u][0] = x.x;
+                    v[u][1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const float ws = __shfl_sync(FULL, w, s + u);
+#pragma unroll
+                for (int e = 0; e < EPL; e++)
+                    acc[e] = fmaf(v[u][e], ws, acc[e]);
+            }
+        }
+        for (; s < n; s++) {
+            const float ws = __shfl_sync(FULL, w, s);
+            const float *src = po + (size_t)(s0 + s) * D;
+#pragma unroll
+            for (int e = 0; e < EPL; e++)
+                acc[e] = fmaf(src[e], ws, acc[e]);
+        }
     }
-    for (int s = 16; s < ns; s++)
-        L += ml[2 * s + 1] * exp2f(ml[2 * s] - M);
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        L += __shfl_xor_sync(FULL, L, o);
     const float inv = 1.0f / L;
-    const float *po = p.part_o + (size_t)row * p.num_splits * D;
-    bf16 *dst = p.out + (size_t)row * D;
-    const bf16 *gt = ((p.flags & NA_OUT_GATE) && p.gate) ? p.gate + (size_t)row * D : nullptr;
-    for (int e = lane * 2; e < D; e += 64) {
-        float o0 = 0.f, o1 = 0.f;
-        for (int s = 0; s < ns; s++) {
-            const float ws = s < 16 ? w[s] : exp2f(ml[2 * s] - M);
-            const float2 v = *reinterpret_cast<const float2 *>(po + (size_t)s * D + e);
-            o0 = fmaf(v.x, ws, o0);
-            o1 = fmaf(v.y, ws, o1);
-        }
-        o0 *= inv;
-        o1 *= inv;
-        if (gt) {
-            const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162 *>(gt + e);
-            o0 *= 1.0f / (1.0f + __expf(-__bfloat162float(g.x)));
-            o1 *= 1.0f / (1.0f + __expf(-__bfloat162float(g.y)));
-        }
-        *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(o0, o1);
+    bf16 *dst = p.out + (size_t)row * D + lane * EPL;
+    float g[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; e++)
+        g[e] = 1.0f;
+    if ((p.flags & NA_OUT_GATE) && p.gate) {
+        const bf16 *gt = p.gate + (size_t)row * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; e++)
+            g[e] = 1.0f / (1.0f + __expf(-__bfloat162float(gt[e])));
     }
+    uint32_t packed[EPL / 2];
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2)
+        packed[e / 2] = pack_bf16x2(acc[e] * inv * g[e], acc[e + 1] * inv * g[e + 1]);
+    if constexpr (EPL == 4)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    else
+        *reinterpret_cast<uint32_t *>(dst) = packed[0];
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -582,13 +729,12 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
         configured = true;
     }
     dim3 grid(p.q_tiles, p.H, p.batch * p.num_splits);
-    prefill_tc_kernel<D><<<grid, THREADS, smem, stream>>>(p, mq, mk, mv);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(prefill_tc_kernel<D>, grid, dim3(THREADS), smem, stream, p, mq, mk, mv);
     if (e != cudaSuccess || p.num_splits == 1)
         return e;
     const int nrows = total_tokens * p.H;
-    prefill_combine_kernel<D><<<(nrows + 7) / 8, 256, 0, stream>>>(p, total_tokens);
-    return cudaGetLastError();
+    return launch_kernel(prefill_combine_kernel<D>, dim3((nrows + 7) / 8), dim3(256), 0, stream, p,
+                         total_tokens);
 }
 
 }  // namespace

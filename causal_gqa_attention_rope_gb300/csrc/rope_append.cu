@@ -217,6 +217,30 @@ __device__ __forceinline__ void rotate(F2 a0, F2 a1, float4 c, float fr, float &
     y1 = fmaf(r1.hi, fr, r1.lo * fr);
 }
 
+// The same for exact inputs (no low parts): a0 cos - a1 sin with both leading
+// products exact (fmaf residuals), their sum error-free, the low parts of cos
+// and sin entering once.
+__device__ __forceinline__ void rotate_exact(float a0, float a1, float4 c, float fr, float &y0,
+                                             float &y1)
+{
+    {
+        const float p0 = a0 * c.x, e0 = fmaf(a0, c.x, -p0);
+        const float p1 = -a1 * c.z, e1 = fmaf(-a1, c.z, -p1);
+        const float s = p0 + p1, bb = s - p0;
+        const float t = (p0 - (s - bb)) + (p1 - bb);
+        const float lo = t + (e0 + e1) + fmaf(a0, c.y, -a1 * c.w);
+        y0 = fmaf(s, fr, lo * fr);
+    }
+    {
+        const float p0 = a0 * c.z, e0 = fmaf(a0, c.z, -p0);
+        const float p1 = a1 * c.x, e1 = fmaf(a1, c.x, -p1);
+        const float s = p0 + p1, bb = s - p0;
+        const float t = (p0 - (s - bb)) + (p1 - bb);
+        const float lo = t + (e0 + e1) + fmaf(a0, c.w, a1 * c.y);
+        y1 = fmaf(s, fr, lo * fr);
+    }
+}
+
 __device__ __forceinline__ const bf16 *row_src(const RopeAppendParams &p, int t, int r)
 {
     if (r < p.H)
@@ -262,6 +286,17 @@ __device__ __forceinline__ void owner_of(const RopeAppendParams &p, int t, int l
     }
 }
 
+// 16-byte read-only load kept where it is written (the compiler may not sink
+// it past the barriers that follow, so its latency overlaps theirs).
+__device__ __forceinline__ uint4 ldg_early(const void *p)
+{
+    uint4 u;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                 : "l"(p));
+    return u;
+}
+
 // ------------------------------------------------------ register path --
 
 constexpr int kMaxUnits = 768;  // one unit per thread: up to 96 rows of d = 128
@@ -299,20 +334,31 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
         e1 = e0 + 8;
     }
 
+    // Constant data and kernel parameters go before the wait: the table, and
+    // this thread's frequency (a dynamically indexed parameter).
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+        reinterpret_cast<uint4 *>(trig)[i] = __ldg(reinterpret_cast<const uint4 *>(&kTrig) + i);
+    unsigned long long fhi = 0;
+    unsigned int flo = 0;
+    if ((int)threadIdx.x < half) {
+        fhi = turns.hi[threadIdx.x];
+        flo = turns.lo[threadIdx.x];
+    }
+    grid_dependency_wait();
+    grid_dependents_launch();
+
     // Everything the token needs is requested first.
     uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, wa = xa, wb = xa;
     if (active) {
         const uint4 *src = reinterpret_cast<const uint4 *>(row_src(p, t, r));
-        xa = __ldg(src + e0 / 8);
-        xb = __ldg(src + e1 / 8);
+        xa = ldg_early(src + e0 / 8);
+        xb = ldg_early(src + e1 / 8);
         if (qk_norm && !is_v) {
             const uint4 *w = reinterpret_cast<const uint4 *>(r < H ? p.qw : p.kw);
-            wa = __ldg(w + e0 / 8);
-            wb = __ldg(w + e1 / 8);
+            wa = ldg_early(w + e0 / 8);
+            wb = ldg_early(w + e1 / 8);
         }
     }
-    for (int i = threadIdx.x; i < 256; i += blockDim.x)
-        reinterpret_cast<uint4 *>(trig)[i] = __ldg(reinterpret_cast<const uint4 *>(&kTrig) + i);
     int b, pos;
     owner_of(p, t, lane, b, pos);
     if (pos < 0 || pos >= p.capacity) {
@@ -321,9 +367,8 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
         return;
     }
     __syncthreads();
-    if ((int)threadIdx.x < half)
-        cs[threadIdx.x] = cos_sin_turns((unsigned)pos, turns.hi[threadIdx.x], turns.lo[threadIdx.x],
-                                        trig);
+    if ((int)threadIdx.x < half)  // stored [i][k] for pair 8k + i: a row's lanes read adjacent entries
+        cs[(threadIdx.x & 7) * 8 + (threadIdx.x >> 3)] = cos_sin_turns((unsigned)pos, fhi, flo, trig);
     __syncthreads();
 
     float a[8], c[8];
@@ -372,9 +417,15 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
         }
         if (rot) {
             const float fr = f * p.rope_scale;  // the attention factor scales rotated dims only
+            if (qk_norm) {
 #pragma unroll
-            for (int i = 0; i < 8; i++)
-                rotate(xa2[i], xb2[i], cs[8 * k + i], fr, ya[i], yb[i]);
+                for (int i = 0; i < 8; i++)
+                    rotate(xa2[i], xb2[i], cs[i * 8 + k], fr, ya[i], yb[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    rotate_exact(a[i], c[i], cs[i * 8 + k], fr, ya[i], yb[i]);
+            }
         } else {
 #pragma unroll
             for (int i = 0; i < 8; i++) {
@@ -413,6 +464,8 @@ __global__ void __launch_bounds__(kStagedThreads) rope_append_staged_kernel(cons
     const int chunks = rows * cpr;
     for (int i = threadIdx.x; i < 256; i += kStagedThreads)
         reinterpret_cast<uint4 *>(trig)[i] = __ldg(reinterpret_cast<const uint4 *>(&kTrig) + i);
+    grid_dependency_wait();
+    grid_dependents_launch();
     int b, pos;
     owner_of(p, t, lane, b, pos);
     if (pos < 0 || pos >= p.capacity) {
@@ -532,10 +585,10 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq
         if (threads < 64)
             threads = 64;
         if (p.d == 128)
-            rope_append_kernel<128><<<p.total_tokens, threads, 0, stream>>>(p, turns);
-        else
-            rope_append_kernel<64><<<p.total_tokens, threads, 0, stream>>>(p, turns);
-        return cudaGetLastError();
+            return launch_kernel(rope_append_kernel<128>, dim3(p.total_tokens), dim3(threads), 0,
+                                 stream, p, turns);
+        return launch_kernel(rope_append_kernel<64>, dim3(p.total_tokens), dim3(threads), 0, stream,
+                             p, turns);
     }
     const size_t smem = rope_append_smem_bytes(p.H, p.KV, p.d, p.rd);
     static size_t configured = 0;
@@ -547,8 +600,8 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq
             return e;
         configured = smem;
     }
-    rope_append_staged_kernel<<<p.total_tokens, kStagedThreads, smem, stream>>>(p, turns);
-    return cudaGetLastError();
+    return launch_kernel(rope_append_staged_kernel, dim3(p.total_tokens), dim3(kStagedThreads), smem,
+                         stream, p, turns);
 }
 
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd)

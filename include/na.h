@@ -129,6 +129,7 @@ int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_
  * query head h attends keys 0 .. pos of kv head h / (H / KV):
  *   out[t][h] = sum_j softmax_j(scale * q_rot[t][h] . k_j) v_j   (* sigmoid(gate[t][h]))
  *
+ *   cu_seqlens    int32 [batch + 1], non-decreasing, cu_seqlens[0] == 0.
  *   cache_lens    int32 [batch]: prior lengths (the same values given to na_rope_append_kv).
  *   total_tokens  HOST copy of cu_seqlens[batch]; 0 is a no-op returning NA_OK.
  *   max_new_len   HOST upper bound of cu_seqlens[b+1] - cu_seqlens[b].
@@ -138,6 +139,9 @@ int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_
  *   out           bf16 [total_tokens][H][d].
  *   workspace     device scratch of at least na_prefill_workspace_size() bytes
  *                 (NULL allowed when that size is 0).
+ *   status        device int32 or NULL: NA_ERR_INVALID_ARG when a new length exceeds
+ *                 max_new_len or cu_seqlens[0] != 0, NA_ERR_CAPACITY when a position
+ *                 reaches max_total_len or the capacity (those rows are not written).
  */
 int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *cu_seqlens,
                           const int32_t *cache_lens, int32_t total_tokens, int32_t max_new_len,
