@@ -128,13 +128,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         sm.abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 1)
+    // A sequence's first query tile always has rows: for it the tensor memory
+    // is taken before the wait and the first copies are issued speculatively.
+    // Other tiles may be empty padding; they check first and leave at once.
+    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
+    const bool eager = qt == 0;
+    if (eager && warp == 1)
         tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
     grid_dependency_wait();
     grid_dependents_launch();
 
     // ------------------------------------------------------------ the tile --
-    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
     const int h = blockIdx.y;
     const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
     const int kvh = h / p.group;
@@ -145,8 +149,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // sequence's tokens start at row 0: those copies are issued before the
     // sequence bounds arrive, overlapping that round trip (a CTA that turns
     // out to have no work waits for them before it exits).
-    const bool early_q = b == 0;
-    if (threadIdx.x == 0) {
+    const bool early_q = eager && b == 0;
+    if (eager && threadIdx.x == 0) {
         if (early_q) {
             mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
             for (int kb = 0; kb < KB; kb++)
@@ -181,21 +185,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (k_begin >= k_end) {
         run = false;
     }
-    if (!run) {  // nothing to attend: let the early copies land, give the tensor memory back
-        if (threadIdx.x == 0) {
-            if (early_q)
-                mbar_wait_bounded(&sm.q_full, 0);
-            mbar_wait_bounded(&sm.k_full[0], 0);
-            mbar_wait_bounded(&sm.v_full[0], 0);
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 1) {
-            tc::fence_after_sync();
-            tc::tmem_dealloc(sm.tmem_base, TMEM_COLS);
+    if (!run) {
+        if (eager) {  // let the early copies land, give the tensor memory back
+            if (threadIdx.x == 0) {
+                if (early_q)
+                    mbar_wait_bounded(&sm.q_full, 0);
+                mbar_wait_bounded(&sm.k_full[0], 0);
+                mbar_wait_bounded(&sm.v_full[0], 0);
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+            if (warp == 1) {
+                tc::fence_after_sync();
+                tc::tmem_dealloc(sm.tmem_base, TMEM_COLS);
+            }
         }
         return;
     }
+    if (!eager && warp == 1)
+        tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
     const int n_tiles = (k_end - k_begin + BN - 1) / BN;
     const int pre = n_tiles < STAGES ? n_tiles : STAGES;  // tiles loaded before the barrier
 
@@ -209,7 +217,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = 0; kb < KB; kb++)
                 tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, tok0 + r0, &sm.q_full);
         }
-        for (int j = 1; j < pre; j++) {
+        for (int j = eager ? 1 : 0; j < pre; j++) {
             mbar_arrive_expect_tx(&sm.k_full[j], KB * BN * 128);
             for (int kb = 0; kb < KB; kb++)
                 tc::tma_load_2d(sm.k[j][kb], &map_k, kb * 64, row_base + j * BN, &sm.k_full[j]);
@@ -445,6 +453,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0)
                 mbar_arrive(&sm.p_full[sb]);
         }
+        // Gate values of this lane's slice of the warp's 32 output rows, all
+        // requested now so their latency overlaps the last P V product
+        // (loaded one row at a time they cost ~25 us per CTA).
+        constexpr int GW = D / 64;  // 32-bit words of gate per lane and row
+        const bool gated = ok && p.num_splits == 1 && (p.flags & NA_OUT_GATE) && p.gate;
+        uint32_t gpre[32][GW];
+        if (gated) {
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                const int rr = quarter * 32 + i;
+                const size_t off = ((size_t)(tok0 + r0 + rr) * p.H + h) * D + lane * 2 * GW;
+                gpre[i][0] = 0;
+                if constexpr (GW == 2)
+                    gpre[i][1] = 0;
+                if (rr < rows) {
+                    if constexpr (GW == 2) {
+                        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p.gate + off));
+                        gpre[i][0] = u.x;
+                        gpre[i][1] = u.y;
+                    } else {
+                        gpre[i][0] = __ldg(reinterpret_cast<const unsigned int *>(p.gate + off));
+                    }
+                }
+            }
+        }
         if (!ok) {
             if (lane == 0)
                 set_abort(&sm.abort_flag, p.status);
@@ -483,12 +516,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 p.part_ml[row * 2 + 1] = l;
             }
             __syncwarp();
-            const bool gated = !split_out && (p.flags & NA_OUT_GATE) && p.gate;
-#pragma unroll 8
-            for (int i = 0; i < 32; i++) {
+            // One row per step, lanes across the row.
+            auto row_out = [&](int i, const uint32_t *gw) {
                 const int rr = quarter * 32 + i;
-                if (rr >= rows)
-                    break;
                 const size_t tok = (size_t)(tok0 + r0 + rr);
                 const float *src = stage + rr * LDS + lane * EPL;
                 float v[EPL];
@@ -509,23 +539,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                         *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
                     else
                         *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
-                } else {
-                    const size_t off = (tok * p.H + h) * D + lane * EPL;
-                    if (gated) {
-                        const bf16 *g = p.gate + off;
-#pragma unroll
-                        for (int e = 0; e < EPL; e++)
-                            v[e] *= 1.0f / (1.0f + __expf(-__bfloat162float(g[e])));
-                    }
-                    uint32_t pk[EPL / 2];
-#pragma unroll
-                    for (int e = 0; e < EPL; e += 2)
-                        pk[e / 2] = pack_bf16x2(v[e], v[e + 1]);
-                    if constexpr (EPL == 4)
-                        *reinterpret_cast<uint2 *>(p.out + off) = make_uint2(pk[0], pk[1]);
-                    else
-                        *reinterpret_cast<uint32_t *>(p.out + off) = pk[0];
+                    return;
                 }
+                if (gw) {
+#pragma unroll
+                    for (int e = 0; e < EPL; e += 2) {
+                        const float g0 = __uint_as_float(gw[e / 2] << 16);
+                        const float g1 = __uint_as_float(gw[e / 2] & 0xffff0000u);
+                        v[e] *= __fdividef(1.0f, 1.0f + __expf(-g0));
+                        v[e + 1] *= __fdividef(1.0f, 1.0f + __expf(-g1));
+                    }
+                }
+                uint32_t pk[EPL / 2];
+#pragma unroll
+                for (int e = 0; e < EPL; e += 2)
+                    pk[e / 2] = pack_bf16x2(v[e], v[e + 1]);
+                const size_t off = (tok * p.H + h) * D + lane * EPL;
+                if constexpr (EPL == 4)
+                    *reinterpret_cast<uint2 *>(p.out + off) = make_uint2(pk[0], pk[1]);
+                else
+                    *reinterpret_cast<uint32_t *>(p.out + off) = pk[0];
+            };
+            const int nrows = min(32, rows - quarter * 32);
+            if (gated) {  // fully unrolled: the prefetched gate words are indexed statically
+#pragma unroll
+                for (int i = 0; i < 32; i++)
+                    if (i < nrows)
+                        row_out(i, gpre[i]);
+            } else {
+#pragma unroll 8
+                for (int i = 0; i < nrows; i++)
+                    row_out(i, nullptr);
             }
         } else if (lane == 0) {
             set_abort(&sm.abort_flag, p.status);
@@ -650,9 +694,19 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
         g[e] = 1.0f;
     if ((p.flags & NA_OUT_GATE) && p.gate) {
         const bf16 *gt = p.gate + (size_t)row * D + lane * EPL;
+        uint32_t gw[EPL / 2];
+        if constexpr (EPL == 4) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(gt));
+            gw[0] = u.x;
+            gw[1] = u.y;
+        } else {
+            gw[0] = __ldg(reinterpret_cast<const unsigned int *>(gt));
+        }
 #pragma unroll
-        for (int e = 0; e < EPL; e++)
-            g[e] = 1.0f / (1.0f + __expf(-__bfloat162float(gt[e])));
+        for (int e = 0; e < EPL; e += 2) {
+            g[e] = __fdividef(1.0f, 1.0f + __expf(-__uint_as_float(gw[e / 2] << 16)));
+            g[e + 1] = __fdividef(1.0f, 1.0f + __expf(-__uint_as_float(gw[e / 2] & 0xffff0000u)));
+        }
     }
     uint32_t packed[EPL / 2];
 #pragma unroll
