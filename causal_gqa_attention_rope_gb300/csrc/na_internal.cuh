@@ -229,7 +229,10 @@ struct PrefillParams {
     float scale_log2;
     int max_new_len;           // host bounds, checked on the device
     int max_total_len;
-    int q_tiles;               // ceil(max_new_len / q tile rows)
+    int total_tokens;          // host copy of cu_seqlens[batch]
+    int pack;                  // query heads of one kv group per tile (a power of two)
+    int tile_tokens;           // tokens per tile: 128 / pack
+    int q_tiles;               // ceil(max_new_len / tile_tokens)
     int split_len;             // keys per KV split (multiple of the key tile), or 0 = no split
     int num_splits;
     uint32_t flags;

@@ -128,21 +128,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         sm.abort_flag = 0;
         fence_barrier_init();
     }
-    // A sequence's first query tile always has rows: for it the tensor memory
-    // is taken before the wait and the first copies are issued speculatively.
+    // A tile that certainly has rows -- a sequence's first, or with a single
+    // sequence any tile below the host-known token count -- takes the tensor
+    // memory before the wait and issues its first copies speculatively.
     // Other tiles may be empty padding; they check first and leave at once.
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const bool eager = qt == 0;
+    const bool eager = qt == 0 || (p.batch == 1 && qt * p.tile_tokens < p.total_tokens);
     if (eager && warp == 1)
         tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
     grid_dependency_wait();
     grid_dependents_launch();
 
     // ------------------------------------------------------------ the tile --
-    const int h = blockIdx.y;
+    // The 128 rows are tile_tokens tokens x pack query heads of one kv group,
+    // token-major: row r is token r >> pack_shift, head h0 + (r & (pack - 1)).
+    const int pack_shift = __ffs(p.pack) - 1;
+    const int h0 = blockIdx.y * p.pack;
     const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
-    const int kvh = h / p.group;
-    const int r0 = qt * BM;
+    const int kvh = h0 / p.group;
+    const int r0 = qt * p.tile_tokens;  // first token of the tile within the sequence
     const int k_begin = p.num_splits > 1 ? split * p.split_len : 0;
     const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
     // The first K and V tiles depend only on the block, and the first
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (early_q) {
             mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
             for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, r0, &sm.q_full);
+                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h0, r0, &sm.q_full);
         }
         mbar_arrive_expect_tx(&sm.k_full[0], KB * BN * 128);
         for (int kb = 0; kb < KB; kb++)
@@ -166,14 +170,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tok0 = __ldg(p.cu_seqlens + b);
     const int n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
     const int prior = __ldg(p.cache_lens + b);
-    const int rows = min(BM, n_new - r0);
-    const int pos_lo = prior + r0, pos_hi = prior + r0 + rows - 1;
+    const int rows_tok = min(p.tile_tokens, n_new - r0);
+    const int rows = rows_tok << pack_shift;  // valid tensor-memory rows
+    const int pos_lo = prior + r0, pos_hi = prior + r0 + rows_tok - 1;
     int k_end = pos_hi + 1;
     if (p.num_splits > 1)
         k_end = min(k_end, k_begin + p.split_len);
     bool run = true;  // uniform over the CTA
     if (n_new > p.max_new_len || (b == 0 && tok0 != 0)) {
-        if (qt == 0 && h == 0 && split == 0 && threadIdx.x == 0)
+        if (qt == 0 && blockIdx.y == 0 && split == 0 && threadIdx.x == 0)
             na_report(p.status, NA_ERR_INVALID_ARG);
         run = false;
     } else if (r0 >= n_new) {
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!early_q) {
             mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
             for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h, tok0 + r0, &sm.q_full);
+                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h0, tok0 + r0, &sm.q_full);
         }
         for (int j = eager ? 1 : 0; j < pre; j++) {
             mbar_arrive_expect_tx(&sm.k_full[j], KB * BN * 128);
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------- softmax --
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // query row == TMEM lane
-        const int row_pos = pos_lo + r;
+        const int row_pos = pos_lo + (r >> pack_shift);
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t o_t = tmem + lane_off;
         const float sl2 = p.scale_log2;
@@ -463,7 +468,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; i++) {
                 const int rr = quarter * 32 + i;
-                const size_t off = ((size_t)(tok0 + r0 + rr) * p.H + h) * D + lane * 2 * GW;
+                const size_t off = ((size_t)(tok0 + r0 + (rr >> pack_shift)) * p.H + h0 +
+                                    (rr & (p.pack - 1))) * D + lane * 2 * GW;
                 gpre[i][0] = 0;
                 if constexpr (GW == 2)
                     gpre[i][1] = 0;
@@ -511,7 +517,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (split_out && r < rows) {
-                const size_t row = ((size_t)(tok0 + r0 + r) * p.H + h) * p.num_splits + split;
+                const size_t row = ((size_t)(tok0 + r0 + (r >> pack_shift)) * p.H + h0 +
+                                    (r & (p.pack - 1))) * p.num_splits + split;
                 p.part_ml[row * 2] = m_ref;
                 p.part_ml[row * 2 + 1] = l;
             }
@@ -519,7 +526,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // One row per step, lanes across the row.
             auto row_out = [&](int i, const uint32_t *gw) {
                 const int rr = quarter * 32 + i;
-                const size_t tok = (size_t)(tok0 + r0 + rr);
+                const size_t tok = (size_t)(tok0 + r0 + (rr >> pack_shift));
+                const int h = h0 + (rr & (p.pack - 1));
                 const float *src = stage + rr * LDS + lane * EPL;
                 float v[EPL];
                 if constexpr (EPL == 4) {
@@ -760,7 +768,7 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
     {
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)total_tokens};
         const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.H * D * 2};
-        const cuuint32_t box[3] = {64, 1, BM};
+        const cuuint32_t box[3] = {64, (cuuint32_t)p.pack, (cuuint32_t)p.tile_tokens};
         if (!make_map(&mq, p.q, 3, dims, strides, box))
             return cudaErrorInvalidValue;
     }
@@ -782,7 +790,7 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
             return e;
         configured = true;
     }
-    dim3 grid(p.q_tiles, p.H, p.batch * p.num_splits);
+    dim3 grid(p.q_tiles, p.H / p.pack, p.batch * p.num_splits);
     cudaError_t e = launch_kernel(prefill_tc_kernel<D>, grid, dim3(THREADS), smem, stream, p, mq, mk, mv);
     if (e != cudaSuccess || p.num_splits == 1)
         return e;

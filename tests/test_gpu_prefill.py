@@ -75,6 +75,17 @@ def test_prefill_short_chunk_long_history_splits_keys(oracle):
     _compare_step(oracle, step, what="split keys")
 
 
+@pytest.mark.parametrize("prior,new", [(0, 200), (300, 37), (5000, 96)])
+def test_prefill_single_sequence_packed_heads(oracle, prior, new):
+    """One sequence whose token count is not a multiple of the 128-row tile:
+    the launch packs the group's query heads into each tile (token-major
+    rows), takes every tile below the token count as certainly non-empty, and
+    (with the long history) splits the keys."""
+    spec = W.Spec(H=8, KV=2, d=128, rd=128, rope=W.RopeParams(base=1e4), out_gate=True)
+    step = W.make_step(spec, [prior], [new], prior + new + 64, seed=57)
+    _compare_step(oracle, step, what=f"packed single {prior}+{new}")
+
+
 def test_prefill_varlen_small_all_rows(oracle):
     """Packed varlen step with qk-norm and gate (the mixed-serving options) at
     a size the oracle checks in full."""
