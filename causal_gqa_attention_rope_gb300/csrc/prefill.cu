@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // memory before the wait and issues its first copies speculatively.
     // Other tiles may be empty padding; they check first and leave at once.
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const bool eager = qt == 0 || (p.batch == 1 && qt * p.tile_tokens < p.total_tokens);
+    const bool eager = p.batch == 1 && qt * p.tile_tokens < p.total_tokens;
     if (eager && warp == 1)
         tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
     grid_dependency_wait();
@@ -144,22 +144,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     // token-major: row r is token r >> pack_shift, head h0 + (r & (pack - 1)).
     const int pack_shift = __ffs(p.pack) - 1;
     const int h0 = blockIdx.y * p.pack;
-    const int b = blockIdx.z / p.num_splits, split = blockIdx.z - b * p.num_splits;
+    const int slot = blockIdx.z / p.num_splits, split = blockIdx.z - slot * p.num_splits;
     const int kvh = h0 / p.group;
     const int r0 = qt * p.tile_tokens;  // first token of the tile within the sequence
     const int k_begin = p.num_splits > 1 ? split * p.split_len : 0;
-    const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
-    // The first K and V tiles depend only on the block, and the first
-    // sequence's tokens start at row 0: those copies are issued before the
-    // sequence bounds arrive, overlapping that round trip (a CTA that turns
-    // out to have no work waits for them before it exits).
-    const bool early_q = eager && b == 0;
-    if (eager && threadIdx.x == 0) {
-        if (early_q) {
-            mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
-            for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h0, r0, &sm.q_full);
+    // The sequence this block serves.  With several sequences (up to 32) the
+    // slots go to sequences in order of decreasing end position (prior + new
+    // tokens), so the longest tiles start first (list scheduling of this
+    // one-CTA-per-SM grid: measured ~10% shorter on mixed lengths).  The
+    // bounds of every sequence come in the same round of loads.
+    int b = slot, tok0, n_new, prior;
+    if (p.batch > 1 && p.batch <= 32) {
+        int c0 = 0, c1 = 0, pl = 0, key = -1;
+        if (lane < p.batch) {
+            c0 = __ldg(p.cu_seqlens + lane);
+            c1 = __ldg(p.cu_seqlens + lane + 1);
+            pl = __ldg(p.cache_lens + lane);
+            key = pl + (c1 - c0);
         }
+        int rank = 0;
+        for (int j = 0; j < p.batch; j++) {
+            const int kj = __shfl_sync(0xffffffffu, key, j);
+            rank += (kj > key) || (kj == key && j < lane);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, lane < p.batch && rank == slot);
+        const int src = __ffs(m) - 1;  // ranks are a permutation of 0 .. batch - 1
+        b = src;
+        tok0 = __shfl_sync(0xffffffffu, c0, src);
+        n_new = __shfl_sync(0xffffffffu, c1, src) - tok0;
+        prior = __shfl_sync(0xffffffffu, pl, src);
+    }
+    const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
+    // With a single sequence the first K and V tiles depend only on the block,
+    // and its tokens start at row 0: those copies are issued before the
+    // sequence bounds arrive, overlapping that round trip (a CTA that turns out
+    // to have no work waits for them before it exits).
+    const bool early_q = eager;
+    if (eager && threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&sm.q_full, KB * BM * 128);
+        for (int kb = 0; kb < KB; kb++)
+            tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h0, r0, &sm.q_full);
         mbar_arrive_expect_tx(&sm.k_full[0], KB * BN * 128);
         for (int kb = 0; kb < KB; kb++)
             tc::tma_load_2d(sm.k[0][kb], &map_k, kb * 64, row_base, &sm.k_full[0]);
@@ -167,9 +191,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kb = 0; kb < KB; kb++)
             tc::tma_load_2d(sm.v[0][kb], &map_v, kb * 64, row_base, &sm.v_full[0]);
     }
-    const int tok0 = __ldg(p.cu_seqlens + b);
-    const int n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
-    const int prior = __ldg(p.cache_lens + b);
+    if (!(p.batch > 1 && p.batch <= 32)) {
+        tok0 = __ldg(p.cu_seqlens + b);
+        n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
+        prior = __ldg(p.cache_lens + b);
+    }
     const int rows_tok = min(p.tile_tokens, n_new - r0);
     const int rows = rows_tok << pack_shift;  // valid tensor-memory rows
     const int pos_lo = prior + r0, pos_hi = prior + r0 + rows_tok - 1;
