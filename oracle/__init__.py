@@ -96,6 +96,9 @@ class Oracle:
             ctypes.c_int, _D, _D, _D, ctypes.c_int, _I, _D, _D, _D, ctypes.c_int,
             ctypes.c_int, _I]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_decode_importance.argtypes = [ctypes.c_int, ctypes.c_int, _D, ctypes.c_int, _I,
+                                                 _D, ctypes.c_int, ctypes.c_int]
+        lib.oracle_decode_importance.restype = None
         self.lib = lib
 
     # --- RoPE frequencies (cortiq fns rope_inv_freq / yarn_inv_freq) ---
@@ -199,6 +202,21 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_decode: length beyond capacity or stride")
         return out, probs
+
+
+    def decode_importance(self, H, probs, kv_lens, imp=None, accumulate=False):
+        """Born-rule importance of a decode step: imp[b][j] (+)= sum over heads of
+        probs[b][h][j] for j < kv_lens[b] (cortiq fn qwen_attention_core).
+        probs [B,H,stride]; returns imp [B,stride] (a new zero array unless given)."""
+        probs = np.ascontiguousarray(probs, dtype=np.float64)
+        B, _, stride = probs.shape
+        kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+        if imp is None:
+            imp = np.zeros((B, stride), dtype=np.float64)
+        out = np.ascontiguousarray(imp, dtype=np.float64).copy()
+        self.lib.oracle_decode_importance(H, B, _dp(probs), stride, _ip(kl), _dp(out),
+                                          out.shape[1], 1 if accumulate else 0)
+        return out
 
 
 _default: Optional[Oracle] = None

@@ -346,3 +346,24 @@ int oracle_decode(int H, int KV, int d, double scale, int flags, int batch, cons
     free(scores);
     return 0;
 }
+
+/* Born-rule importance of one decode step (cortiq fn qwen_attention_core: each
+ * head's probabilities are summed into `imp`, which cache.accumulate_imp adds
+ * to the position's running importance; fn attend_all_heads returns the same
+ * sum): imp[b][j] = sum over the H query heads of probs[b][h][j], for
+ * j < kv_lens[b]; with accumulate the sum is added to what imp holds.  Keys
+ * past kv_lens[b] are left untouched. */
+void oracle_decode_importance(int H, int batch, const double *probs, int probs_stride,
+                              const int *kv_lens, double *imp, int imp_stride, int accumulate)
+{
+    for (int b = 0; b < batch; b++) {
+        int n = kv_lens[b];
+        for (int j = 0; j < n; j++) {
+            double s = 0.0;
+            for (int h = 0; h < H; h++)
+                s += probs[((size_t)b * H + h) * (size_t)probs_stride + j];
+            double *dst = imp + (size_t)b * imp_stride + j;
+            *dst = accumulate ? *dst + s : s;
+        }
+    }
+}

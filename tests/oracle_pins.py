@@ -388,4 +388,46 @@ def pin_norm_before_rope_in_append(o):
     assert np.all(ck[0, 0, untouched] == 99.0) and np.all(cv[0, 0, untouched] == 99.0)
 
 
+def pin_importance_sums_and_brute_force(o):
+    """Born-rule importance (cortiq fn qwen_attention_core sums every head's
+    probabilities per key): against per-head scipy softmax summed by hand; each
+    sequence's importance totals H (every head's probabilities sum to 1), an
+    empty sequence gets none, keys past the length stay untouched, and
+    accumulation adds to what the buffer holds."""
+    rng = np.random.default_rng(13)
+    B, H, KV, d, cap = 3, 6, 3, 8, 9
+    lens = [9, 0, 4]
+    q = rng.standard_normal((B, H, d))
+    ck = rng.standard_normal((B, KV, cap, d))
+    cv = rng.standard_normal((B, KV, cap, d))
+    _, probs = o.decode(H, KV, d, 0.4, 0, q, ck, cv, lens, probs_stride=cap)
+    imp = o.decode_importance(H, probs, lens)
+    for b in range(B):
+        n = lens[b]
+        want = np.zeros(cap)
+        for h in range(H):
+            g = h // (H // KV)
+            if n:
+                want[:n] += scipy_softmax(0.4 * ck[b, g, :n] @ q[b, h])
+        _close(imp[b], want, 1e-13, f"importance {b}")
+        assert abs(imp[b].sum() - (H if n else 0)) < 1e-12
+    prev = rng.standard_normal((B, cap))
+    acc = o.decode_importance(H, probs, lens, imp=prev, accumulate=True)
+    for b in range(B):
+        n = lens[b]
+        _close(acc[b, :n], prev[b, :n] + imp[b, :n], 1e-14, "accumulate")
+        _close(acc[b, n:], prev[b, n:], 0.0, "untouched tail")
+
+
+def pin_importance_page_uniform(o):
+    """The pages' uniform example (identical keys: every probability 1/3)
+    gives importance H/3 on every key."""
+    H, KV, d = 4, 1, 3
+    q = np.ones((1, H, d))
+    ck = np.ones((1, KV, 3, d))
+    cv = np.eye(3).reshape(1, KV, 3, d)
+    _, probs = o.decode(H, KV, d, 1.0, 0, q, ck, cv, [3], probs_stride=3)
+    _close(o.decode_importance(H, probs, [3])[0], np.full(3, H / 3.0), 1e-14, "uniform")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

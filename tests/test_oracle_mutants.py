@@ -34,6 +34,9 @@ MUTANTS = [
     ("k_not_normed", "oracle_rmsnorm_head(kx, k_norm_w, d, eps, zc);", "(void)zc;", 1),
     ("v_norm_on_k", "oracle_vnorm_head(vx, d, eps);", "oracle_vnorm_head(kx, d, eps);", 1),
     ("probs_before_shift_lost", "scores[j] = exp(scores[j] - m);", "scores[j] = exp(scores[j] - m) + 1e-3;", 1),
+    ("importance_mean_not_sum", "*dst = accumulate ? *dst + s : s;", "*dst = accumulate ? *dst + s / H : s / H;", 1),
+    ("importance_first_head_only", "for (int h = 0; h < H; h++)\n                s += probs[", "for (int h = 0; h < 1; h++)\n                s += probs[", 1),
+    ("importance_overwrites", "*dst = accumulate ? *dst + s : s;", "*dst = s;", 1),
 ]
 
 
