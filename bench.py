@@ -469,6 +469,34 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
     assert int(status.item()) == 0
     ms, kms = statistics.mean(times), statistics.mean(kd)
     ach = alg_bytes / (kms * 1e-3) / 1e9
+
+    # Born-rule importance of the step, accumulated into a running per-key
+    # buffer (reads every head's probabilities, reads and writes the buffer).
+    imp = torch.zeros(B, max_kv, dtype=torch.float32, device=dev)
+    imp_bytes = sum(lens) * (H * 4 + 2 * 4)
+    for _ in range(warmup):
+        na.na_decode_importance(cfg, probs, kv_lens, max_kv, imp, accumulate=True, status=status)
+    torch.cuda.synchronize()
+    it = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        na.na_decode_importance(cfg, probs, kv_lens, max_kv, imp, accumulate=True, status=status)
+        b.record()
+        torch.cuda.synchronize()
+        it.append(a.elapsed_time(b))
+    assert int(status.item()) == 0
+    ims = statistics.mean(it)
+    iach = imp_bytes / (ims * 1e-3) / 1e9
+    importance = {"workload": "importance_" + wl.name, "metric": "importance GB/s", "unit": "GB/s",
+                  "value": iach, "ms_per_step": ims, "bytes_per_step": imp_bytes,
+                  "roofline": {"bound": "hbm", "achieved": iach, "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": iach / peaks["hbm_gbs"],
+                               "traffic": traffic_from_profiles("importance.cu",
+                                                                "importance_" + wl.name),
+                               "kernel": "na_decode_importance",
+                               "peak_source": peaks["source"] + " HBM copy"}}
     return {"workload": wl.name, "metric": "decode KV GB/s", "unit": "GB/s",
             "value": (alg_bytes + B * 3 * KV * d * 2) / (ms * 1e-3) / 1e9, "ms_per_step": ms,
             "bytes_per_step": alg_bytes,
@@ -476,7 +504,8 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
                          "frac": ach / peaks["hbm_gbs"],
                          "traffic": traffic_from_profiles("decode.cu", wl.name),
                          "kernel": "na_attn_decode (split pass + combine)",
-                         "peak_source": peaks["source"] + " HBM copy"}}
+                         "peak_source": peaks["source"] + " HBM copy"},
+            "importance": importance}
 
 
 # ---------------------------------------------------- oracle (CPU) timing --
@@ -572,7 +601,9 @@ def main():
     r = bench_chunked(wl, args.steps, args.warmup, peaks, flush)
     extra = []
     if not args.no_extra:
-        extra.append(bench_decode(W.C3, args.steps, args.warmup, peaks, flush))
+        dec_rec = bench_decode(W.C3, args.steps, args.warmup, peaks, flush)
+        extra.append({k: v for k, v in dec_rec.items() if k != "importance"})
+        extra.append(dec_rec["importance"])
         extra.append(bench_varlen(W.C5, args.steps, args.warmup, peaks, flush))
         r4 = bench_chunked(W.C4, max(2, args.steps // 4), min(args.warmup, 3), peaks, flush,
                            with_e2e=False)

@@ -37,8 +37,8 @@ NA_OUT_GATE = 8
 
 # Every symbol include/na.h declares.
 EXPORTED = ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
-            "na_attn_decode_static_ws", "na_prefill_workspace_size", "na_decode_workspace_size",
-            "na_status_string")
+            "na_attn_decode_static_ws", "na_decode_importance", "na_prefill_workspace_size",
+            "na_decode_workspace_size", "na_status_string")
 
 
 class na_attn_cfg(ctypes.Structure):
@@ -87,12 +87,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.na_attn_decode.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, I32, P, SZ, P, P]
     lib.na_attn_decode_static_ws.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, I32, P,
                                              P]
+    lib.na_decode_importance.argtypes = [cfgp, I32, P, I32, P, I32, P, I32, I32, P, P]
     lib.na_prefill_workspace_size.argtypes = [cfgp, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_decode_workspace_size.argtypes = [cfgp, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_status_string.argtypes = [ctypes.c_int]
     lib.na_status_string.restype = ctypes.c_char_p
     for name in ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
-                 "na_attn_decode_static_ws", "na_prefill_workspace_size",
+                 "na_attn_decode_static_ws", "na_decode_importance", "na_prefill_workspace_size",
                  "na_decode_workspace_size"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -263,6 +264,19 @@ def na_attn_decode_static_ws(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, ma
                                       _ptr(probs), stride, int(num_splits), _ptr(status),
                                       _stream(stream))
     _check("na_attn_decode_static_ws", rc)
+
+
+def na_decode_importance(cfg: AttnConfig, probs, kv_lens, max_kv_len: int, imp,
+                         accumulate: bool = False, status=None, stream=None):
+    """Born-rule importance of a decode step: imp[b][j] (+)= sum over heads of
+    probs[b][h][j] for j < kv_lens[b].  probs [B,H,stride] fp32, imp [B,stride2]."""
+    lib = load_library()
+    c = cfg.c()
+    rc = lib.na_decode_importance(ctypes.byref(c), int(probs.shape[0]), _ptr(probs),
+                                  int(probs.shape[-1]), _ptr(kv_lens), int(max_kv_len), _ptr(imp),
+                                  int(imp.shape[-1]), 1 if accumulate else 0, _ptr(status),
+                                  _stream(stream))
+    _check("na_decode_importance", rc)
 
 
 def workspace(nbytes: int, device="cuda"):

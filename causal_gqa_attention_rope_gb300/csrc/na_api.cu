@@ -340,6 +340,34 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
                : NA_ERR_CUDA;
 }
 
+int na_decode_importance(const na_attn_cfg *cfg, int32_t batch, const float *probs,
+                         int32_t probs_stride, const int32_t *kv_lens, int32_t max_kv_len,
+                         float *imp, int32_t imp_stride, int32_t accumulate, int32_t *status,
+                         void *stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc != NA_OK)
+        return rc;
+    if (batch <= 0 || max_kv_len < 0 || !probs || !kv_lens || !imp)
+        return NA_ERR_INVALID_ARG;
+    if (max_kv_len > probs_stride || max_kv_len > imp_stride)
+        return NA_ERR_CAPACITY;
+    ImportanceParams p{};
+    p.H = cfg->num_heads;
+    p.batch = batch;
+    p.max_kv_len = max_kv_len;
+    p.probs_stride = probs_stride;
+    p.imp_stride = imp_stride;
+    p.accumulate = accumulate != 0;
+    p.vector_ok = aligned16(probs) && aligned16(imp) && probs_stride % 4 == 0 && imp_stride % 4 == 0;
+    p.probs = probs;
+    p.kv_lens = kv_lens;
+    p.imp = imp;
+    p.status = status;
+    return launch_importance(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NA_OK
+                                                                                   : NA_ERR_CUDA;
+}
+
 int na_decode_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t max_kv_len,
                              int32_t num_splits, size_t *bytes)
 {

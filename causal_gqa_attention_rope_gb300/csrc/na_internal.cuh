@@ -244,10 +244,22 @@ struct PrefillParams {
     int32_t *status;
 };
 
+struct ImportanceParams {
+    int H, batch, max_kv_len;
+    long long probs_stride, imp_stride;
+    int accumulate;
+    int vector_ok;             // 16-byte aligned rows: float4 loads and stores
+    const float *probs;
+    const int32_t *kv_lens;
+    float *imp;
+    int32_t *status;
+};
+
 // Kernel launchers (one translation unit each).
 cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq, int half,
                                cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int d, int heads_per_cta, cudaStream_t stream);
+cudaError_t launch_importance(const ImportanceParams &p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, int cache_batch,
                            cudaStream_t stream);
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd);

@@ -207,6 +207,30 @@ int na_attn_decode_static_ws(const na_attn_cfg *cfg, int32_t batch, const void *
                              const void *gate, void *out, float *probs, int32_t probs_stride,
                              int32_t num_splits, int32_t *status, void *stream);
 
+/*
+ * Born-rule importance of a decode step: the probability mass that reads each key.
+ * [cortiq fn qwen_attention_core: each head's per-key probabilities are summed into
+ *  `imp`, which cache.accumulate_imp adds to the position's running importance for
+ *  importance-aware eviction; fn attend_all_heads returns the same sum.]
+ *
+ *   imp[b][j] = sum over the H query heads of probs[b][h][j]     for j < kv_lens[b]
+ * or, with accumulate != 0, imp[b][j] += that sum.  Keys past kv_lens[b] are not
+ * touched.  The sum runs over heads in index order in fp32 (deterministic).
+ *
+ *   probs       fp32 [batch][H][probs_stride]: the probabilities na_attn_decode wrote.
+ *   kv_lens     int32 [batch] (device), the same lengths given to na_attn_decode.
+ *   max_kv_len  HOST upper bound of kv_lens; <= probs_stride and <= imp_stride.
+ *   imp         fp32 [batch][imp_stride] (device), caller-owned.
+ *   status      device int32 or NULL: NA_ERR_CAPACITY for a length past max_kv_len
+ *               (that sequence is skipped).
+ * Errors: NA_ERR_INVALID_ARG for null buffers or a non-positive batch,
+ * NA_ERR_CAPACITY when max_kv_len exceeds a stride.
+ */
+int na_decode_importance(const na_attn_cfg *cfg, int32_t batch, const float *probs,
+                         int32_t probs_stride, const int32_t *kv_lens, int32_t max_kv_len,
+                         float *imp, int32_t imp_stride, int32_t accumulate, int32_t *status,
+                         void *stream);
+
 /* Workspace bytes (HOST out-parameter) that na_attn_prefill_chunk needs for these bounds. */
 int na_prefill_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t total_tokens,
                               int32_t max_new_len, int32_t max_total_len, size_t *bytes);

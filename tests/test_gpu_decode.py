@@ -103,3 +103,78 @@ def test_full_decode_b64_h32kv8_kv512to8192(oracle):
         b, h = divmod(r, H)
         assert_out_close(out[b, h].double().numpy(), ref_out[b, h], f"row {r}")
         assert_probs_close(probs[b, h, :lens[b]].numpy(), ref_p[b, h, :lens[b]], f"probs {r}")
+
+
+# ----------------------------------------------------- Born-rule importance --
+
+def _gpu_importance(dec, probs_cpu, imp_init, accumulate):
+    import causal_gqa_attention_rope_gb300 as na
+    from harness import attn_cfg
+    dev = "cuda"
+    imp = imp_init.clone().to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    max_kv = int(dec.kv_lens.max())
+    na.na_decode_importance(attn_cfg(dec.spec), probs_cpu.to(dev), dec.kv_lens.to(dev), max_kv,
+                            imp, accumulate=accumulate, status=status)
+    torch.cuda.synchronize()
+    return imp.cpu(), int(status.item())
+
+
+def _check_importance(oracle, dec, probs_stride=None, accumulate=False):
+    """GPU importance of the GPU probabilities against the oracle's importance
+    of the oracle's probabilities: each probability is within PROBS_MAX_ABS, so
+    each sum over H heads is within H * PROBS_MAX_ABS."""
+    from harness import PROBS_MAX_ABS
+    s = dec.spec
+    _, probs, st = gpu_decode(dec, probs_stride=probs_stride)
+    assert st == 0
+    B, stride = probs.shape[0], probs.shape[-1]
+    init = torch.full((B, stride), 0.25, dtype=torch.float32)
+    if accumulate:
+        init = torch.rand((B, stride), generator=torch.Generator().manual_seed(3))
+    got, st = _gpu_importance(dec, probs, init, accumulate)
+    assert st == 0
+    _, ref_p = _oracle_decode(oracle, dec, stride=stride)
+    ref = oracle.decode_importance(s.H, ref_p, dec.kv_lens.numpy(),
+                                   imp=init.double().numpy(), accumulate=accumulate)
+    lens = dec.kv_lens.tolist()
+    for b, n in enumerate(lens):
+        err = float(np.max(np.abs(got[b, :n].double().numpy() - ref[b, :n]))) if n else 0.0
+        assert err <= s.H * PROBS_MAX_ABS, f"importance b{b}: {err:.3e}"
+        assert torch.equal(got[b, n:], init[b, n:]), "importance written past kv_len"
+
+
+@pytest.mark.parametrize("stride", [None, 1539])
+def test_decode_importance(oracle, stride):
+    """Sum over heads of the per-key probabilities (vector path; and an odd
+    stride, the scalar path), empty and one-key sequences included."""
+    dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128), [0, 1, 3, 700, 1500], 1536, seed=97)
+    _check_importance(oracle, dec, probs_stride=stride)
+
+
+def test_decode_importance_accumulates(oracle):
+    dec = W.make_decode(W.Spec(H=16, KV=2, d=64, rd=64), [5, 64, 333], 512, seed=98)
+    _check_importance(oracle, dec, accumulate=True)
+
+
+def test_full_decode_importance_b64_h32kv8(oracle):
+    """Importance of the full decode workload: every sequence totals H (each
+    head's probabilities sum to one), and two sampled sequences match the
+    oracle key by key."""
+    from harness import PROBS_MAX_ABS
+    dec = W.make_decode_workload(W.C3, seed=0)
+    _, probs, st = gpu_decode(dec)
+    assert st == 0
+    B, H, stride = probs.shape
+    got, st = _gpu_importance(dec, probs, torch.zeros(B, stride), False)
+    assert st == 0
+    lens = dec.kv_lens.tolist()
+    for b, n in enumerate(lens):
+        assert abs(float(got[b, :n].double().sum()) - H) < 1e-2, f"total b{b}"
+    for b in sample_rows(B, 2, seed=17):
+        rows = [b * H + h for h in range(H)]
+        _, ref_p = _oracle_decode(oracle, dec, rows_bh=rows, stride=stride)
+        ref = oracle.decode_importance(H, ref_p[b:b + 1], dec.kv_lens.numpy()[b:b + 1])
+        n = lens[b]
+        err = float(np.max(np.abs(got[b, :n].double().numpy() - ref[0, :n])))
+        assert err <= H * PROBS_MAX_ABS, f"importance b{b}: {err:.3e}"
