@@ -89,12 +89,13 @@ class Oracle:
         lib.oracle_rope_append.restype = ctypes.c_int
         lib.oracle_attend_rows.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-            ctypes.c_int, _I, _I, _D, _D, _D, ctypes.c_int, _D, ctypes.c_int, _I, _D]
+            ctypes.c_int, _I, _I, _D, _D, _D, ctypes.c_int, _D, ctypes.c_int, _I, _D,
+            ctypes.c_double, ctypes.c_int]
         lib.oracle_attend_rows.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
             ctypes.c_int, _D, _D, _D, ctypes.c_int, _I, _D, _D, _D, ctypes.c_int,
-            ctypes.c_int, _I]
+            ctypes.c_int, _I, ctypes.c_double, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_decode_importance.argtypes = [ctypes.c_int, ctypes.c_int, _D, ctypes.c_int, _I,
                                                  _D, ctypes.c_int, ctypes.c_int]
@@ -167,8 +168,9 @@ class Oracle:
         return q_out
 
     def attend_rows(self, H, KV, d, scale, flags, cu_seqlens, cache_lens, q_rot, cache_k,
-                    cache_v, gate, rows: Sequence[int]):
-        """Causal attention output for the listed new-token rows: [len(rows), H, d]."""
+                    cache_v, gate, rows: Sequence[int], softcap: float = 0.0, window: int = 0):
+        """Causal attention output for the listed new-token rows: [len(rows), H, d]
+        (softcap > 0 caps the scores; window > 0 keeps only the last keys)."""
         cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
         cl = np.ascontiguousarray(cache_lens, dtype=np.int32)
         r = np.ascontiguousarray(rows, dtype=np.int32)
@@ -177,13 +179,14 @@ class Oracle:
         rc = self.lib.oracle_attend_rows(H, KV, d, scale, flags, len(cu) - 1, _ip(cu), _ip(cl),
                                          _dp(np.ascontiguousarray(q_rot)), _dp(cache_k),
                                          _dp(cache_v), cache_k.shape[2], _dp(g), len(r), _ip(r),
-                                         _dp(out))
+                                         _dp(out), float(softcap), int(window))
         if rc != 0:
             raise ValueError("oracle_attend_rows: bad row or position")
         return out
 
     def decode(self, H, KV, d, scale, flags, q, cache_k, cache_v, kv_lens, gate=None,
-               want_probs=True, probs_stride=None, rows_bh: Optional[Sequence[int]] = None):
+               want_probs=True, probs_stride=None, rows_bh: Optional[Sequence[int]] = None,
+               softcap: float = 0.0, window: int = 0):
         """Single-token decode.  Returns (out [B,H,d], probs [B,H,stride] or None).
         With rows_bh only those (b*H+h) rows are computed (others stay zero)."""
         B = q.shape[0]
@@ -198,7 +201,7 @@ class Oracle:
                                     _dp(np.ascontiguousarray(q, dtype=np.float64)), _dp(cache_k),
                                     _dp(cache_v), cache_k.shape[2], _ip(kl), _dp(g), _dp(out),
                                     _dp(probs), probs_stride, 0 if rb is None else len(rb),
-                                    _ip(rb))
+                                    _ip(rb), float(softcap), int(window))
         if rc != 0:
             raise ValueError("oracle_decode: length beyond capacity or stride")
         return out, probs

@@ -226,32 +226,45 @@ int oracle_rope_append(int H, int KV, int d, int rd, int flags, double eps,
 
 /* ------------------------------------------------------------ attend --- */
 
-/* cortiq fn attention_head, one query against keys [0, n) of one KV head:
- *   s_j = scale * q.k_j;  p_j = exp(s_j - max s) / sum;  o = sum_j p_j v_j.
- * `scores` is scratch of length n; when `probs` is non-NULL it receives p_j.
- * n == 0 leaves o at zero and writes no probabilities. */
-static void attend_one(const double *q, const double *keys, const double *vals, int n, int d,
-                       double scale, double *scores, double *o, double *probs)
+/* cortiq fn attention_head, one query against keys [first, n) of one KV head:
+ *   s_j = scale * q.k_j, capped to c * tanh(s_j / c) when softcap c > 0
+ *   (QwenAttnCfg.softcap: Gemma-2 logit soft-capping, scores pass tanh(s/c)*c
+ *   before the softmax);  p_j = exp(s_j - max s) / sum;  o = sum_j p_j v_j.
+ * Keys before `first` are outside a sliding window (QwenAttnCfg.window, fn
+ * attend_all_heads: first = stored - window) and get probability 0.
+ * `scores` is scratch of length n; when `probs` is non-NULL it receives p_j
+ * for j < n.  n == 0 leaves o at zero and writes no probabilities. */
+static void attend_one(const double *q, const double *keys, const double *vals, int n, int first,
+                       int d, double scale, double softcap, double *scores, double *o,
+                       double *probs)
 {
     for (int i = 0; i < d; i++)
         o[i] = 0.0;
     if (n <= 0)
         return;
+    if (first < 0)
+        first = 0;
     double m = -INFINITY;
-    for (int j = 0; j < n; j++) {
+    for (int j = first; j < n; j++) {
         double s = 0.0;
         for (int i = 0; i < d; i++)
             s += q[i] * keys[(size_t)j * d + i];
-        scores[j] = s * scale;
+        s *= scale;
+        if (softcap > 0.0)
+            s = softcap * tanh(s / softcap);
+        scores[j] = s;
         if (scores[j] > m)
             m = scores[j];
     }
     double sum = 0.0;
-    for (int j = 0; j < n; j++) {
+    for (int j = first; j < n; j++) {
         scores[j] = exp(scores[j] - m);
         sum += scores[j];
     }
-    for (int j = 0; j < n; j++) {
+    if (probs)
+        for (int j = 0; j < first; j++)
+            probs[j] = 0.0;
+    for (int j = first; j < n; j++) {
         double p = scores[j] / sum;
         if (probs)
             probs[j] = p;
@@ -271,13 +284,15 @@ static void apply_gate(double *o, const double *g, int d)
  * cortiq fn qwen_attention_batch, portable attend): the chunk's keys are
  * already in the cache; new token t of sequence b sits at
  * pos = cache_lens[b] + (t - cu_seqlens[b]) and attends keys 0..pos
- * inclusive of its own KV head kvh = h / (H / KV).  Computed for the listed
- * token indices only: out[r][h][d] for rows[r].  Returns 0, or -1 on a bad
- * row or a position past the capacity. */
+ * inclusive of its own KV head kvh = h / (H / KV) -- only the last `window`
+ * of them when window > 0 -- with scores soft-capped when softcap > 0.
+ * Computed for the listed token indices only: out[r][h][d] for rows[r].
+ * Returns 0, or -1 on a bad row or a position past the capacity. */
 int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
                        const int *cu_seqlens, const int *cache_lens, const double *q_rot,
                        const double *cache_k, const double *cache_v, int capacity,
-                       const double *gate, int nrows, const int *rows, double *out)
+                       const double *gate, int nrows, const int *rows, double *out,
+                       double softcap, int window)
 {
     int group = H / KV;
     double *scores = (double *)malloc(sizeof(double) * (size_t)(capacity > 0 ? capacity : 1));
@@ -300,8 +315,8 @@ int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
             const double *qv = q_rot + ((size_t)t * H + h) * d;
             double *o = out + ((size_t)r * H + h) * d;
             attend_one(qv, cache_k + cache_index(b, kvh, 0, KV, capacity, d),
-                       cache_v + cache_index(b, kvh, 0, KV, capacity, d), pos + 1, d, scale,
-                       scores, o, NULL);
+                       cache_v + cache_index(b, kvh, 0, KV, capacity, d), pos + 1,
+                       window > 0 ? pos + 1 - window : 0, d, scale, softcap, scores, o, NULL);
             if ((flags & ORACLE_OUT_GATE) && gate)
                 apply_gate(o, gate + ((size_t)t * H + h) * d, d);
         }
@@ -315,12 +330,13 @@ int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
  * of KV head h / (H / KV).  out [B][H][d]; probs [B][H][probs_stride] receives
  * the per-key probabilities when non-NULL.  Only the first `nrows` (b, h)
  * pairs listed in rows_bh (b * H + h) are computed when rows_bh is non-NULL;
- * otherwise all of them.  Returns 0, or -1 when a length exceeds the
- * capacity or the probability stride. */
+ * otherwise all of them.  With window > 0 only the last `window` keys are
+ * attended (the others get probability 0); softcap > 0 caps the scores.
+ * Returns 0, or -1 when a length exceeds the capacity or the stride. */
 int oracle_decode(int H, int KV, int d, double scale, int flags, int batch, const double *q,
                   const double *cache_k, const double *cache_v, int capacity,
                   const int *kv_lens, const double *gate, double *out, double *probs,
-                  int probs_stride, int nrows, const int *rows_bh)
+                  int probs_stride, int nrows, const int *rows_bh, double softcap, int window)
 {
     int group = H / KV;
     double *scores = (double *)malloc(sizeof(double) * (size_t)(capacity > 0 ? capacity : 1));
@@ -338,7 +354,8 @@ int oracle_decode(int H, int KV, int d, double scale, int flags, int batch, cons
         int kvh = h / group;
         double *o = out + ((size_t)b * H + h) * d;
         attend_one(q + ((size_t)b * H + h) * d, cache_k + cache_index(b, kvh, 0, KV, capacity, d),
-                   cache_v + cache_index(b, kvh, 0, KV, capacity, d), n, d, scale, scores, o,
+                   cache_v + cache_index(b, kvh, 0, KV, capacity, d), n,
+                   window > 0 ? n - window : 0, d, scale, softcap, scores, o,
                    probs ? probs + ((size_t)b * H + h) * (size_t)probs_stride : NULL);
         if ((flags & ORACLE_OUT_GATE) && gate && n > 0)
             apply_gate(o, gate + ((size_t)b * H + h) * d, d);

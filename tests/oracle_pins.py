@@ -430,4 +430,73 @@ def pin_importance_page_uniform(o):
     _close(o.decode_importance(H, probs, [3])[0], np.full(3, H / 3.0), 1e-14, "uniform")
 
 
+def pin_softcap(o):
+    """Logit soft-capping (QwenAttnCfg.softcap: scores pass tanh(s/c)*c before
+    the softmax): against library softmax of c*tanh(scale q.k / c); a huge cap
+    is plain attention; capped scores never leave (-c, c)."""
+    rng = np.random.default_rng(21)
+    B, H, KV, d, cap = 2, 4, 2, 8, 10
+    lens = [10, 6]
+    q = 3.0 * rng.standard_normal((B, H, d))
+    ck = rng.standard_normal((B, KV, cap, d))
+    cv = rng.standard_normal((B, KV, cap, d))
+    c = 2.0
+    out, probs = o.decode(H, KV, d, 0.5, 0, q, ck, cv, lens, probs_stride=cap, softcap=c)
+    plain_out, plain_p = o.decode(H, KV, d, 0.5, 0, q, ck, cv, lens, probs_stride=cap)
+    huge_out, huge_p = o.decode(H, KV, d, 0.5, 0, q, ck, cv, lens, probs_stride=cap, softcap=1e12)
+    for b in range(B):
+        n = lens[b]
+        for h in range(H):
+            g = h // (H // KV)
+            s = 0.5 * ck[b, g, :n] @ q[b, h]
+            p = scipy_softmax(c * np.tanh(s / c))
+            _close(probs[b, h, :n], p, 1e-14, "capped probs")
+            _close(out[b, h], p @ cv[b, g, :n], 1e-13, "capped out")
+            # a cap of 2 bounds the probability ratio by e^(2c)
+            assert probs[b, h, :n].max() / probs[b, h, :n].min() < math.exp(2 * c) + 1e-9
+    _close(huge_p, plain_p, 1e-12, "huge cap probs")
+    _close(huge_out, plain_out, 1e-12, "huge cap out")
+
+
+def pin_sliding_window(o):
+    """Sliding window (QwenAttnCfg.window; fn attend_all_heads attends from
+    stored - window): against a brute-force softmax over the last W keys, keys
+    before the window get probability 0, W >= n is full attention, W = 1 gives
+    exactly the newest value; in prefill, row pos sees keys pos-W+1 .. pos (a
+    windowed prefill row equals windowed decode at that position)."""
+    rng = np.random.default_rng(22)
+    B, H, KV, d, cap = 2, 2, 1, 8, 9
+    lens = [9, 4]
+    q = rng.standard_normal((B, H, d))
+    ck = rng.standard_normal((B, KV, cap, d))
+    cv = rng.standard_normal((B, KV, cap, d))
+    W = 3
+    out, probs = o.decode(H, KV, d, 0.7, 0, q, ck, cv, lens, probs_stride=cap, window=W)
+    full_out, full_p = o.decode(H, KV, d, 0.7, 0, q, ck, cv, lens, probs_stride=cap, window=50)
+    plain_out, plain_p = o.decode(H, KV, d, 0.7, 0, q, ck, cv, lens, probs_stride=cap)
+    one_out, one_p = o.decode(H, KV, d, 0.7, 0, q, ck, cv, lens, probs_stride=cap, window=1)
+    for b in range(B):
+        n = lens[b]
+        lo = max(0, n - W)
+        for h in range(H):
+            p = scipy_softmax(0.7 * ck[b, 0, lo:n] @ q[b, h])
+            _close(probs[b, h, lo:n], p, 1e-14, "window probs")
+            _close(probs[b, h, :lo], np.zeros(lo), 0.0, "outside window")
+            _close(out[b, h], p @ cv[b, 0, lo:n], 1e-13, "window out")
+            _close(one_out[b, h], cv[b, 0, n - 1], 0.0, "window 1 value")
+            _close(one_p[b, h, :n], np.eye(n)[n - 1], 0.0, "window 1 probs")
+    _close(full_out, plain_out, 0.0, "window >= n")
+    _close(full_p, plain_p, 0.0, "window >= n probs")
+    # prefill rows against decode at the same positions
+    L = 7
+    qs = rng.standard_normal((L, H, d))
+    kc = rng.standard_normal((1, KV, L, d))
+    vc = rng.standard_normal((1, KV, L, d))
+    rows = o.attend_rows(H, KV, d, 0.7, 0, [0, L], [0], qs, kc, vc, None, list(range(L)),
+                         window=W)
+    for t in range(L):
+        dec, _ = o.decode(H, KV, d, 0.7, 0, qs[t:t + 1], kc, vc, [t + 1], window=W)
+        _close(rows[t], dec[0], 1e-14, f"prefill row {t}")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

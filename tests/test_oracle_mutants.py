@@ -18,10 +18,10 @@ MUTANTS = [
      "inv_freq[i] = extrap * (1.0 - extrapolation) + interp * extrapolation;", 1),
     ("yarn_low_ceil", "double lo = floor(", "double lo = ceil(", 1),
     ("yarn_factor_multiplies", "double interp = extrap / factor;", "double interp = extrap * factor;", 1),
-    ("causal_excludes_self", "pos + 1, d, scale,", "pos, d, scale,", 1),
+    ("causal_excludes_self", "capacity, d), pos + 1,\n", "capacity, d), pos,\n", 1),
     ("gqa_modulo_mapping", "int kvh = h / group;", "int kvh = h % KV;", 2),
     ("softmax_unnormalised", "double p = scores[j] / sum;", "double p = scores[j];", 1),
-    ("score_scale_dropped", "scores[j] = s * scale;", "scores[j] = s;", 1),
+    ("score_scale_dropped", "        s *= scale;\n", "", 1),
     ("rms_sum_not_mean", "double inv = 1.0 / sqrt(ss / (double)d + eps);\n    for (int i = 0; i < d; i++)\n        x[i] = x[i] * inv",
      "double inv = 1.0 / sqrt(ss + eps);\n    for (int i = 0; i < d; i++)\n        x[i] = x[i] * inv", 1),
     ("vnorm_eps_dropped", "double inv = 1.0 / sqrt(ss / (double)d + eps);\n    for (int i = 0; i < d; i++)\n        x[i] *= inv;",
@@ -36,6 +36,9 @@ MUTANTS = [
     ("probs_before_shift_lost", "scores[j] = exp(scores[j] - m);", "scores[j] = exp(scores[j] - m) + 1e-3;", 1),
     ("importance_mean_not_sum", "*dst = accumulate ? *dst + s : s;", "*dst = accumulate ? *dst + s / H : s / H;", 1),
     ("importance_first_head_only", "for (int h = 0; h < H; h++)\n                s += probs[", "for (int h = 0; h < 1; h++)\n                s += probs[", 1),
+    ("softcap_missing_divide", "s = softcap * tanh(s / softcap);", "s = softcap * tanh(s);", 1),
+    ("decode_window_off_by_one", "window > 0 ? n - window : 0", "window > 0 ? n - window + 1 : 0", 1),
+    ("prefill_window_off_by_one", "window > 0 ? pos + 1 - window : 0", "window > 0 ? pos - window : 0", 1),
     ("importance_overwrites", "*dst = accumulate ? *dst + s : s;", "*dst = s;", 1),
 ]
 
