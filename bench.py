@@ -199,7 +199,8 @@ def attn_cfg(spec: W.Spec):
     return na.AttnConfig(num_heads=spec.H, num_kv_heads=spec.KV, head_dim=spec.d,
                          rotary_dim=spec.rd, sm_scale=spec.sm_scale, rms_eps=spec.eps,
                          qk_norm=spec.qk_norm, qk_norm_zero_centered=spec.qk_norm_zero_centered,
-                         v_norm=spec.v_norm, out_gate=spec.out_gate)
+                         v_norm=spec.v_norm, out_gate=spec.out_gate, softcap=spec.softcap,
+                         window=spec.window)
 
 
 def rope_cfg(spec: W.Spec):

@@ -45,7 +45,8 @@ class na_attn_cfg(ctypes.Structure):
     _fields_ = [("num_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("softcap", ctypes.c_float),
+                ("window", ctypes.c_int32)]
 
 
 class na_rope_params(ctypes.Structure):
@@ -118,6 +119,8 @@ class AttnConfig:
     qk_norm_zero_centered: bool = False
     v_norm: bool = False
     out_gate: bool = False
+    softcap: float = 0.0
+    window: int = 0
 
     @property
     def flags(self) -> int:
@@ -128,7 +131,7 @@ class AttnConfig:
     def c(self) -> na_attn_cfg:
         rd = self.head_dim if self.rotary_dim is None else self.rotary_dim
         return na_attn_cfg(self.num_heads, self.num_kv_heads, self.head_dim, rd, self.sm_scale,
-                           self.rms_eps, self.flags)
+                           self.rms_eps, self.flags, self.softcap, self.window)
 
 
 @dataclass

@@ -51,12 +51,26 @@ constexpr int KPS = 32 / LPK;              // keys per warp step
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 
-// Keys of sequence b, or 0 for a length past the cache capacity or the host
-// bound (skipped here, reported by the combine pass).
-__device__ __forceinline__ int valid_len(const DecodeParams &p, int b)
+// Keys of sequence b that are attended -- the last `window` of its length, or
+// all of them without a window -- with *first the index of the first one; 0
+// for a length past the cache capacity or the host bound (skipped here,
+// reported by the combine pass).
+__device__ __forceinline__ int attended_keys(const DecodeParams &p, int b, int &first)
 {
     const int n = __ldg(p.kv_lens + b);
-    return (n < 0 || n > p.capacity || n > p.max_kv_len) ? 0 : n;
+    if (n < 0 || n > p.capacity || n > p.max_kv_len) {
+        first = 0;
+        return 0;
+    }
+    const int len = (p.window > 0 && n > p.window) ? p.window : n;
+    first = n - len;
+    return len;
+}
+
+__device__ __forceinline__ int valid_len(const DecodeParams &p, int b)
+{
+    int first;
+    return attended_keys(p, b, first);
 }
 
 // Where this CTA's key slice starts: computed by one full warp, then shared.
@@ -83,6 +97,7 @@ struct DecSmem {
 // One piece: the keys [k0, k1) of stream (b, kvh, hc) that this CTA reads.
 struct Piece {
     int b, kvh, hc, k0, k1, id;
+    int kf;            // cache index of the stream's first attended key
     bool first, last;  // holds the stream's first / last key
 };
 
@@ -140,7 +155,7 @@ __device__ __forceinline__ void locate_slice(const DecodeParams &p, int lane, Sl
 // Walks this CTA's pieces in order; every thread of the CTA walks the same way.
 struct Walker {
     long long start, end, off;
-    int b, si, len, spb, c;
+    int b, si, len, kfirst, spb, c;
     bool done;
 
     __device__ __forceinline__ void init(const Slice &sl, const DecodeParams &p)
@@ -153,19 +168,20 @@ struct Walker {
         spb = p.KV * p.head_chunks;
         c = blockIdx.x;
         done = sl.empty != 0;
-        len = done ? 0 : valid_len(p, b);
+        kfirst = 0;
+        len = done ? 0 : attended_keys(p, b, kfirst);
     }
 
     __device__ __forceinline__ bool next(const DecodeParams &p, Piece &pc)
     {
         while (!done && b < p.batch && off < end) {
             const long long s_off = off;
-            const int n = len, sb = b, ssi = si;
+            const int n = len, sb = b, ssi = si, kfs = kfirst;
             off += n;
             if (++si == spb) {
                 si = 0;
                 if (++b < p.batch)
-                    len = valid_len(p, b);
+                    len = attended_keys(p, b, kfirst);
             }
             const long long lo = start > s_off ? start - s_off : 0;
             const long long hi = end - s_off < n ? end - s_off : n;
@@ -176,6 +192,7 @@ struct Walker {
                 pc.k0 = (int)lo;
                 pc.k1 = (int)hi;
                 pc.id = sb * spb + ssi + c;
+                pc.kf = kfs;
                 pc.first = lo == 0;
                 pc.last = hi == n;
                 return true;
@@ -208,7 +225,7 @@ __device__ __forceinline__ void load_words(const bf16 *src, uint32_t (&w)[N])
     }
 }
 
-template <int D, int HPC>
+template <int D, int HPC, bool CAPPED>
 __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const DecodeParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -257,9 +274,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
                 const int n = min(DEC_TILE, s1 - j0);
                 const uint32_t bytes = (uint32_t)(n * D * (int)sizeof(bf16));
                 mbar_arrive_expect_tx(&sm.full[stage], 2 * bytes);
-                bulk_copy_g2s(sm.k[stage], p.cache_k + head_base + (size_t)j0 * D, bytes,
+                bulk_copy_g2s(sm.k[stage], p.cache_k + head_base + (size_t)(pc.kf + j0) * D, bytes,
                               &sm.full[stage], policy);
-                bulk_copy_g2s(sm.v[stage], p.cache_v + head_base + (size_t)j0 * D, bytes,
+                bulk_copy_g2s(sm.v[stage], p.cache_v + head_base + (size_t)(pc.kf + j0) * D, bytes,
                               &sm.full[stage], policy);
             }
         }
@@ -372,9 +389,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
                     }
                 }
                 const int j = j0 + kl;
-                s[st] = (full_tile || j < s1) ? part[0] : -INFINITY;
+                float sc = part[0];
+                if constexpr (CAPPED) {  // c tanh(s / c) in the log2 domain, tanh(y) = 1 - 2 / (e^2y + 1)
+                    const float e = exp2f(sc * p.cap_in);
+                    sc = p.cap_out * (1.0f - __fdividef(2.0f, e + 1.0f));
+                }
+                s[st] = (full_tile || j < s1) ? sc : -INFINITY;
                 if (probs_row && (full_tile || j < s1) && (sub % R) == 0)
-                    probs_row[j] = part[0];
+                    probs_row[pc.kf + j] = sc;
             }
             // Tile maximum per head, then (rarely) raise the reference maximum.
             float tmax = s[0];
@@ -562,45 +584,55 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
         out[e] = __float2bfloat16_rn(o);
     }
     if (p.probs) {
+        // keys before the window (none without one) get probability 0
+        const int kf = (p.window > 0 && n > p.window) ? n - p.window : 0;
         float *pr = p.probs + (size_t)bh * p.probs_stride;
+        auto prob = [&](float raw, int j) { return j < kf ? 0.f : exp2f(raw - M) * inv_l; };
         if ((p.probs_stride & 3) == 0) {
             const int n4 = n >> 2;
             float4 *pr4 = reinterpret_cast<float4 *>(pr);
             for (int i = threadIdx.x; i < n4; i += blockDim.x) {
                 float4 x = pr4[i];
-                x.x = exp2f(x.x - M) * inv_l;
-                x.y = exp2f(x.y - M) * inv_l;
-                x.z = exp2f(x.z - M) * inv_l;
-                x.w = exp2f(x.w - M) * inv_l;
+                x.x = prob(x.x, 4 * i);
+                x.y = prob(x.y, 4 * i + 1);
+                x.z = prob(x.z, 4 * i + 2);
+                x.w = prob(x.w, 4 * i + 3);
                 pr4[i] = x;
             }
             for (int j = (n4 << 2) + threadIdx.x; j < n; j += blockDim.x)
-                pr[j] = exp2f(pr[j] - M) * inv_l;
+                pr[j] = prob(pr[j], j);
         } else {
             for (int j = threadIdx.x; j < n; j += blockDim.x)
-                pr[j] = exp2f(pr[j] - M) * inv_l;
+                pr[j] = prob(pr[j], j);
         }
     }
 }
 
-template <int D, int HPC>
-cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
+template <int D, int HPC, bool CAPPED>
+cudaError_t launch_split(const DecodeParams &p, cudaStream_t stream)
 {
     const size_t smem = sizeof(DecSmem<D, HPC>);
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, HPC>,
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, HPC, CAPPED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_split_kernel<D, HPC>,
+            e = cudaFuncSetAttribute(decode_split_kernel<D, HPC, CAPPED>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    cudaError_t e = launch_kernel(decode_split_kernel<D, HPC>, dim3(p.grid), dim3(DEC_THREADS), smem,
-                                  stream, p);
+    return launch_kernel(decode_split_kernel<D, HPC, CAPPED>, dim3(p.grid), dim3(DEC_THREADS), smem,
+                         stream, p);
+}
+
+template <int D, int HPC>
+cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
+{
+    cudaError_t e = p.cap_out > 0.f ? launch_split<D, HPC, true>(p, stream)
+                                    : launch_split<D, HPC, false>(p, stream);
     if (e != cudaSuccess)
         return e;
     return launch_kernel(decode_combine_kernel<D>, dim3(p.batch * p.H), dim3(256), 0, stream, p);

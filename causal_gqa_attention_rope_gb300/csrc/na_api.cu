@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <cmath>
+
 #include "na_internal.cuh"
 
 namespace {
@@ -24,6 +26,8 @@ int check_cfg(const na_attn_cfg *c)
     if (c->flags & ~kKnownFlags)
         return NA_ERR_INVALID_ARG;
     if (!(c->rms_eps >= 0.f))
+        return NA_ERR_INVALID_ARG;
+    if (!(c->softcap >= 0.f) || !std::isfinite(c->softcap) || c->window < 0)
         return NA_ERR_INVALID_ARG;
     if (c->head_dim != 64 && c->head_dim != 128)
         return NA_ERR_UNSUPPORTED;
@@ -134,21 +138,29 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     pl.q_tiles = (max_new_len + pl.tile_tokens - 1) / pl.tile_tokens;
     const long long est = (long long)batch * pl.q_tiles * (c->num_heads / pl.pack);
     const long long target = sm_count();
+    // Keys one tile can see: all history, or with a sliding window at most the
+    // window plus the tile's own tokens (from the key tile holding the first
+    // row's window start).
+    long long span = max_total_len;
+    if (c->window > 0) {
+        const long long w = (long long)c->window + pl.tile_tokens - 1 + bn;
+        span = w < span ? w : span;
+    }
     int splits = 1;
-    if (est < target && max_total_len > 4 * bn) {
+    if (est < target && span > 4 * bn) {
         splits = (int)(target / est);
-        const int max_by_len = (max_total_len + 4 * bn - 1) / (4 * bn);
+        const int max_by_len = (int)((span + 4 * bn - 1) / (4 * bn));
         splits = splits < max_by_len ? splits : max_by_len;
         if (splits < 1)
             splits = 1;
     }
     if (splits > 1) {
-        int len = (max_total_len + splits - 1) / splits;
+        int len = (int)((span + splits - 1) / splits);
         len = (len + bn - 1) / bn * bn;
         pl.split_len = len;
-        pl.num_splits = (max_total_len + len - 1) / len;
+        pl.num_splits = (int)((span + len - 1) / len);
     } else {
-        pl.split_len = max_total_len > 0 ? max_total_len : 1;
+        pl.split_len = span > 0 ? (int)span : 1;
         pl.num_splits = 1;
     }
     pl.ws_bytes = pl.num_splits > 1
@@ -315,6 +327,8 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
     p.max_new_len = max_new_len;
     p.max_total_len = max_total_len;
     p.total_tokens = total_tokens;
+    p.softcap = cfg->softcap;
+    p.window = cfg->window;
     p.pack = pl.pack;
     p.tile_tokens = pl.tile_tokens;
     p.q_tiles = pl.q_tiles;
@@ -419,6 +433,11 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     p.max_pieces = pl.max_pieces;
     p.max_kv_len = max_kv_len;
     p.flags = cfg->flags;
+    p.window = cfg->window;
+    if (cfg->softcap > 0.f) {  // scores are log2-domain: c tanh(s / c) -> tanh via 2^(2 s / c)
+        p.cap_in = 2.0f / cfg->softcap;
+        p.cap_out = cfg->softcap * 1.4426950408889634f;
+    }
     p.q = static_cast<const bf16 *>(q_rot);
     p.cache_k = static_cast<const bf16 *>(cache->k);
     p.cache_v = static_cast<const bf16 *>(cache->v);

@@ -213,6 +213,8 @@ struct DecodeParams {
     int max_pieces;            // streams + grid: bound on piece ids
     int max_kv_len;            // host bound on kv_lens (checked on the device)
     uint32_t flags;
+    int window;                // > 0: only the last `window` keys are attended
+    float cap_in, cap_out;     // soft-capping of log2-domain scores (cap_out 0: off)
     const bf16 *q, *cache_k, *cache_v, *gate;
     const int32_t *kv_lens;
     bf16 *out;
@@ -230,6 +232,8 @@ struct PrefillParams {
     int max_new_len;           // host bounds, checked on the device
     int max_total_len;
     int total_tokens;          // host copy of cu_seqlens[batch]
+    float softcap;             // > 0: scores capped to softcap * tanh(s / softcap)
+    int window;                // > 0: keys pos - window + 1 .. pos only
     int pack;                  // query heads of one kv group per tile (a power of two)
     int tile_tokens;           // tokens per tile: 128 / pack
     int q_tiles;               // ceil(max_new_len / tile_tokens)

@@ -32,6 +32,7 @@
 // With three S buffers the tensor core computes S_{j+1} and S_{j+2} while the
 // softmax works on tile j, and PV_j runs while it prepares P_{j+1}.
 //
+#include <climits>
 #include <cuda.h>
 #include <mutex>
 
@@ -92,7 +93,7 @@ __device__ __forceinline__ float ex2_mufu(float x)
     return r;
 }
 
-template <int D>
+template <int D, bool CAPPED>
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // memory before the wait and issues its first copies speculatively.
     // Other tiles may be empty padding; they check first and leave at once.
     const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const bool eager = p.batch == 1 && qt * p.tile_tokens < p.total_tokens;
+    const bool eager = p.batch == 1 && p.window == 0 && qt * p.tile_tokens < p.total_tokens;
     if (eager && warp == 1)
         tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
     grid_dependency_wait();
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int slot = blockIdx.z / p.num_splits, split = blockIdx.z - slot * p.num_splits;
     const int kvh = h0 / p.group;
     const int r0 = qt * p.tile_tokens;  // first token of the tile within the sequence
-    const int k_begin = p.num_splits > 1 ? split * p.split_len : 0;
+    const int split_off = p.num_splits > 1 ? split * p.split_len : 0;
     // The sequence this block serves.  With several sequences (up to 32) the
     // slots go to sequences in order of decreasing end position (prior + new
     // tokens), so the longest tiles start first (list scheduling of this
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         n_new = __shfl_sync(0xffffffffu, c1, src) - tok0;
         prior = __shfl_sync(0xffffffffu, pl, src);
     }
-    const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
+    const int spec_row = (b * p.KV + kvh) * p.capacity + split_off;  // tile 0 without a window
     // With a single sequence the first K and V tiles depend only on the block,
     // and its tokens start at row 0: those copies are issued before the
     // sequence bounds arrive, overlapping that round trip (a CTA that turns out
@@ -186,10 +187,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h0, r0, &sm.q_full);
         mbar_arrive_expect_tx(&sm.k_full[0], KB * BN * 128);
         for (int kb = 0; kb < KB; kb++)
-            tc::tma_load_2d(sm.k[0][kb], &map_k, kb * 64, row_base, &sm.k_full[0]);
+            tc::tma_load_2d(sm.k[0][kb], &map_k, kb * 64, spec_row, &sm.k_full[0]);
         mbar_arrive_expect_tx(&sm.v_full[0], KB * BN * 128);
         for (int kb = 0; kb < KB; kb++)
-            tc::tma_load_2d(sm.v[0][kb], &map_v, kb * 64, row_base, &sm.v_full[0]);
+            tc::tma_load_2d(sm.v[0][kb], &map_v, kb * 64, spec_row, &sm.v_full[0]);
     }
     if (!(p.batch > 1 && p.batch <= 32)) {
         tok0 = __ldg(p.cu_seqlens + b);
@@ -199,6 +200,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int rows_tok = min(p.tile_tokens, n_new - r0);
     const int rows = rows_tok << pack_shift;  // valid tensor-memory rows
     const int pos_lo = prior + r0, pos_hi = prior + r0 + rows_tok - 1;
+    // Keys the tile can see: from the key tile holding the first row's window
+    // start (0 without a window) to the last row; splits cut that range.
+    const int win_tile = p.window > 0 ? max(0, pos_lo - p.window + 1) / BN * BN : 0;
+    const int k_begin = win_tile + split_off;
+    const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
     int k_end = pos_hi + 1;
     if (p.num_splits > 1)
         k_end = min(k_end, k_begin + p.split_len);
@@ -363,6 +369,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // query row == TMEM lane
         const int row_pos = pos_lo + (r >> pack_shift);
+        const int row_lo = p.window > 0 ? row_pos - p.window + 1 : INT_MIN;  // first visible key
+        constexpr bool capped = CAPPED;
+        // soft-capped scores, kept in the raw score's units so the rest of the
+        // softmax is unchanged: s' = (c / scale) tanh(s scale / c), with
+        // tanh(y) = 1 - 2 / (e^(2y) + 1)
+        const float cap_in = capped ? 2.0f * p.scale_log2 / p.softcap : 0.f;
+        const float cap_out = capped ? p.softcap * NA_LOG2E / p.scale_log2 : 0.f;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t o_t = tmem + lane_off;
         const float sl2 = p.scale_log2;
@@ -383,14 +396,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc::tmem_ld32(s_t + c * 32, sr[c]);
             tc::tmem_wait_ld();
 
-            const bool need_mask = (j0 + BN - 1 > pos_lo) || (j0 + BN > k_end);
+            if constexpr (capped) {
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        const float e = ex2_mufu(__uint_as_float(sr[c][i]) * cap_in);
+                        sr[c][i] = __float_as_uint(cap_out * (1.0f - __fdividef(2.0f, e + 1.0f)));
+                    }
+            }
+            const bool need_mask = (j0 + BN - 1 > pos_lo) || (j0 + BN > k_end) || (j0 < row_lo);
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < 4; c++)
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
                         const int key = j0 + c * 32 + i;
-                        if (key > row_pos || key >= k_end)
+                        if (key > row_pos || key >= k_end || key < row_lo)
                             sr[c][i] = __float_as_uint(-INFINITY);
                     }
             }
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     const float2 ml0 = lane < p.num_splits ? *reinterpret_cast<const float2 *>(ml + 2 * lane)
                                            : make_float2(-INFINITY, 0.f);
     // Owner sequence: the last b with cu_seqlens[b] <= t, a warp at a time.
-    int b = 0, pos = -1;
+    int b = 0, pos = -1, rt = 0;  // rt: the token's index within its sequence
     for (int base = 0; base < p.batch; base += 32) {
         const int i = base + lane;
         int cu = 0x7fffffff, cl = 0;
@@ -650,14 +672,22 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
         if (m) {
             const int src = 31 - __clz(m);
             b = base + src;
-            pos = __shfl_sync(FULL, cl, src) + (t - __shfl_sync(FULL, cu, src));
+            rt = t - __shfl_sync(FULL, cu, src);
+            pos = __shfl_sync(FULL, cl, src) + rt;
         }
         if (m != FULL)
             break;
     }
     if (pos < 0 || pos >= p.capacity || pos >= p.max_total_len)
         return;  // reported by the split pass
-    const int ns = min(p.num_splits, pos / p.split_len + 1);
+    // Splits start at the key tile holding the window start of the row's query
+    // tile (0 without a window), as in the split pass.
+    int win_tile = 0;
+    if (p.window > 0) {
+        const int tile_pos_lo = pos - rt % p.tile_tokens;
+        win_tile = max(0, tile_pos_lo - p.window + 1) / BN * BN;
+    }
+    const int ns = min(p.num_splits, (pos - win_tile) / p.split_len + 1);
 
     // Global maximum and sum over the splits this row has keys in.
     float M = -INFINITY;
@@ -810,14 +840,21 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
     const size_t smem = tc_smem_bytes<D>();
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<D, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
     dim3 grid(p.q_tiles, p.H / p.pack, p.batch * p.num_splits);
-    cudaError_t e = launch_kernel(prefill_tc_kernel<D>, grid, dim3(THREADS), smem, stream, p, mq, mk, mv);
+    cudaError_t e = p.softcap > 0.f
+                        ? launch_kernel(prefill_tc_kernel<D, true>, grid, dim3(THREADS), smem, stream,
+                                        p, mq, mk, mv)
+                        : launch_kernel(prefill_tc_kernel<D, false>, grid, dim3(THREADS), smem,
+                                        stream, p, mq, mk, mv);
     if (e != cudaSuccess || p.num_splits == 1)
         return e;
     const int nrows = total_tokens * p.H;

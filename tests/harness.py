@@ -72,7 +72,8 @@ def attn_cfg(spec: W.Spec):
     return na.AttnConfig(num_heads=spec.H, num_kv_heads=spec.KV, head_dim=spec.d,
                          rotary_dim=spec.rd, sm_scale=spec.sm_scale, rms_eps=spec.eps,
                          qk_norm=spec.qk_norm, qk_norm_zero_centered=spec.qk_norm_zero_centered,
-                         v_norm=spec.v_norm, out_gate=spec.out_gate)
+                         v_norm=spec.v_norm, out_gate=spec.out_gate, softcap=spec.softcap,
+                         window=spec.window)
 
 
 def rope_cfg(spec: W.Spec):
@@ -222,7 +223,8 @@ def oracle_rows(o, step: W.StepInputs, ost: OracleStep, rows: Sequence[int]) -> 
     s = step.spec
     return o.attend_rows(s.H, s.KV, s.d, score_scale(s), oracle_flags(s),
                          step.cu_seqlens.numpy(), step.cache_lens.numpy(), ost.q_rot,
-                         ost.cache_k, ost.cache_v, W.bf16_to_f64(step.gate), list(rows))
+                         ost.cache_k, ost.cache_v, W.bf16_to_f64(step.gate), list(rows),
+                         softcap=s.softcap, window=s.window)
 
 
 def prompt_as_step(prompt: W.ChunkedPrompt) -> W.StepInputs:

@@ -52,6 +52,10 @@ def _cfg(**kw):
     (dict(rotary_dim=63), na.NA_ERR_INVALID_ARG),
     (dict(rotary_dim=130), na.NA_ERR_INVALID_ARG),
     (dict(head_dim=96, rotary_dim=96), na.NA_ERR_UNSUPPORTED),
+    (dict(softcap=-1.0), na.NA_ERR_INVALID_ARG),
+    (dict(softcap=float("nan")), na.NA_ERR_INVALID_ARG),
+    (dict(softcap=float("inf")), na.NA_ERR_INVALID_ARG),
+    (dict(window=-3), na.NA_ERR_INVALID_ARG),
 ])
 def test_bad_config_rejected_before_launch(lib, kw, code):
     c = _cfg(**kw)

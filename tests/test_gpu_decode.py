@@ -15,7 +15,8 @@ def _oracle_decode(oracle, dec, rows_bh=None, stride=None):
     return oracle.decode(s.H, s.KV, s.d, score_scale(s), oracle_flags(s), W.bf16_to_f64(dec.q),
                          np.ascontiguousarray(W.bf16_to_f64(dec.cache_k)),
                          np.ascontiguousarray(W.bf16_to_f64(dec.cache_v)), dec.kv_lens.numpy(),
-                         gate=W.bf16_to_f64(dec.gate), probs_stride=stride, rows_bh=rows_bh)
+                         gate=W.bf16_to_f64(dec.gate), probs_stride=stride, rows_bh=rows_bh,
+                         softcap=s.softcap, window=s.window)
 
 
 def _check(oracle, dec, num_splits=0, with_probs=True):
@@ -61,6 +62,20 @@ def test_decode_balanced_slices_skip_empty_sequences(oracle, splits):
     lens = [0] * 37 + [3000] + [1, 0] * 15 + [0, 257, 0]
     dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128), lens, 3072, seed=93)
     _check(oracle, dec, num_splits=splits)
+
+
+@pytest.mark.parametrize("name,spec", [
+    ("softcap", W.Spec(H=8, KV=2, d=128, rd=128, softcap=20.0, std=2.0)),
+    ("window256", W.Spec(H=8, KV=2, d=128, rd=128, window=256)),
+    ("window1_d64_gate", W.Spec(H=16, KV=2, d=64, rd=64, window=1, out_gate=True)),
+    ("window_softcap_mha", W.Spec(H=4, KV=4, d=128, rd=128, window=700, softcap=6.0)),
+])
+def test_decode_softcap_and_window(oracle, name, spec):
+    """Soft-capped scores and sliding windows in the split/combine decode, with
+    probabilities (0 before the window) and their importance."""
+    dec = W.make_decode(spec, [0, 1, 5, 256, 257, 1500], 1536, seed=101)
+    _check(oracle, dec)
+    _check_importance(oracle, dec)
 
 
 def test_decode_without_probs(oracle):

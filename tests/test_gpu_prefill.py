@@ -86,6 +86,35 @@ def test_prefill_single_sequence_packed_heads(oracle, prior, new):
     _compare_step(oracle, step, what=f"packed single {prior}+{new}")
 
 
+CAPPED_WINDOWED = {
+    # unit-scale inputs (the tolerance's regime) with a cap small enough to bend
+    # the scores (|s| ~ 1..4 against c = 2)
+    "softcap2_group4": (W.Spec(H=8, KV=2, d=128, rd=128, softcap=2.0), [0, 300], [70, 140]),
+    "softcap_d64_qknorm_gate": (W.Spec(H=6, KV=3, d=64, rd=64, softcap=5.0, qk_norm=True,
+                                       out_gate=True), [17, 0], [40, 9]),
+    "window200_varlen": (W.Spec(H=8, KV=2, d=128, rd=128, window=200), [1000, 30, 0], [300, 5, 130]),
+    "window1_single": (W.Spec(H=4, KV=1, d=128, rd=128, window=1), [20], [40]),
+    "window_and_softcap_mha": (W.Spec(H=3, KV=3, d=64, rd=32, window=77, softcap=8.0), [400], [150]),
+}
+
+
+@pytest.mark.parametrize("name", list(CAPPED_WINDOWED))
+def test_prefill_softcap_and_window(oracle, name):
+    """Logit soft-capping and sliding-window attention against the oracle."""
+    spec, prior, new = CAPPED_WINDOWED[name]
+    cap = max(p + n for p, n in zip(prior, new)) + 8
+    step = W.make_step(spec, prior, new, cap, seed=71)
+    _compare_step(oracle, step, what=name)
+
+
+def test_prefill_window_long_history_splits(oracle):
+    """A short chunk behind a long history with a window: the key range starts at
+    the window, and the launch splits it across CTAs."""
+    spec = W.Spec(H=4, KV=1, d=128, rd=128, window=1500)
+    step = W.make_step(spec, [6000], [24], 6100, seed=73)
+    _compare_step(oracle, step, what="window + splits")
+
+
 def test_prefill_varlen_small_all_rows(oracle):
     """Packed varlen step with qk-norm and gate (the mixed-serving options) at
     a size the oracle checks in full."""

@@ -57,6 +57,8 @@ class Spec:
     norm_w_mean: float = 1.0    # norm weights ~ N(norm_w_mean, norm_w_std)
     norm_w_std: float = 0.1
     sm_scale: float = 0.0       # <= 0: 1/sqrt(d)
+    softcap: float = 0.0        # > 0: logit soft-capping
+    window: int = 0             # > 0: sliding-window attention
 
 
 @dataclass
