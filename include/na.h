@@ -64,8 +64,9 @@ typedef struct na_attn_cfg {
     float sm_scale;        /* score scale; <= 0 selects 1 / sqrt(head_dim) */
     float rms_eps;         /* epsilon of the qk-norm and v-norm */
     uint32_t flags;        /* NA_* option bits */
-    float softcap;         /* > 0: scores pass softcap * tanh(s / softcap) before the softmax
-                              (cortiq QwenAttnCfg.softcap, Gemma-2 logit soft-capping); 0: off */
+    float softcap;         /* > 0: each scaled score s becomes softcap * tanh(s / softcap)
+                              ahead of the softmax (cortiq QwenAttnCfg.softcap, the Gemma-2
+                              soft cap on attention logits); 0: off */
     int32_t window;        /* > 0: a query at pos attends only keys pos - window + 1 .. pos
                               (cortiq QwenAttnCfg.window, sliding window); 0: full context */
 } na_attn_cfg;

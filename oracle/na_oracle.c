@@ -227,9 +227,9 @@ int oracle_rope_append(int H, int KV, int d, int rd, int flags, double eps,
 /* ------------------------------------------------------------ attend --- */
 
 /* cortiq fn attention_head, one query against keys [first, n) of one KV head:
- *   s_j = scale * q.k_j, capped to c * tanh(s_j / c) when softcap c > 0
- *   (QwenAttnCfg.softcap: Gemma-2 logit soft-capping, scores pass tanh(s/c)*c
- *   before the softmax);  p_j = exp(s_j - max s) / sum;  o = sum_j p_j v_j.
+ *   s_j = scale * q.k_j, replaced by c * tanh(s_j / c) when softcap c > 0
+ *   (QwenAttnCfg.softcap, the Gemma-2 soft cap on attention logits, applied
+ *   ahead of the softmax);  p_j = exp(s_j - max s) / sum;  o = sum_j p_j v_j.
  * Keys before `first` are outside a sliding window (QwenAttnCfg.window, fn
  * attend_all_heads: first = stored - window) and get probability 0.
  * `scores` is scratch of length n; when `probs` is non-NULL it receives p_j

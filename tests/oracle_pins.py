@@ -431,8 +431,8 @@ def pin_importance_page_uniform(o):
 
 
 def pin_softcap(o):
-    """Logit soft-capping (QwenAttnCfg.softcap: scores pass tanh(s/c)*c before
-    the softmax): against library softmax of c*tanh(scale q.k / c); a huge cap
+    """Logit soft-capping (QwenAttnCfg.softcap: each scaled score s becomes
+    c*tanh(s/c) ahead of the softmax): against library softmax of c*tanh(scale q.k / c); a huge cap
     is plain attention; capped scores never leave (-c, c)."""
     rng = np.random.default_rng(21)
     B, H, KV, d, cap = 2, 4, 2, 8, 10
