@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
-    ap.add_argument("--only", choices=["chunked", "decode", "varlen", "yarn"], default=None,
+    ap.add_argument("--only", choices=["chunked", "decode", "varlen", "yarn", "pair"], default=None,
                     help="time one workload and print its record (profiling runs)")
     return ap.parse_args()
 
@@ -509,6 +509,55 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
             "importance": importance}
 
 
+def bench_pair_verify(steps, warmup, peaks, flush):
+    """Speculative pair verify: every sequence of the decode workload checks two
+    drafted tokens (a 2-token chunk after kv_len - 2 cached ones).  HBM-bound:
+    the K/V of each (sequence, kv head) is streamed once for both tokens and
+    all query heads of the group (GQA-packed tiles)."""
+    import causal_gqa_attention_rope_gb300 as na
+    wl = W.C3
+    s = wl.spec
+    gen = torch.Generator().manual_seed(3)
+    lens = W.draw_lengths(gen, wl.batch, *wl.kv_range)
+    step = W.make_step(s, [n - 2 for n in lens], [2] * wl.batch, wl.capacity, seed=5)
+    dev = "cuda"
+    cfg = attn_cfg(s)
+    cu, cl = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
+    q = step.q.to(dev)
+    out = torch.empty_like(q)
+    cache = na.KVCache(step.cache_k.to(dev), step.cache_v.to(dev))
+    T, mt = int(step.cu_seqlens[-1]), max(lens)
+    ws = na.workspace(na.na_prefill_workspace_size(cfg, wl.batch, T, 2, mt), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run():
+        na.na_attn_prefill_chunk(cfg, cu, cl, 2, mt, q, cache, out, workspace=ws, status=status)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    assert int(status.item()) == 0
+    ms = statistics.mean(ts)
+    kv_bytes = sum(lens) * s.KV * s.d * 2 * 2
+    ach = kv_bytes / (ms * 1e-3) / 1e9
+    name = "pair_verify_b64_h32kv8d128_kv512to8192"
+    return {"workload": name, "metric": "pair verify KV GB/s", "unit": "GB/s", "value": ach,
+            "ms_per_step": ms, "bytes_per_step": kv_bytes,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "na_attn_prefill_chunk (2-token chunks, GQA-packed tiles)",
+                         "peak_source": peaks["source"] + " HBM copy"}}
+
+
 # ---------------------------------------------------- oracle (CPU) timing --
 
 def cpu_baseline_chunked(wl: W.PrefillWorkload, budget_s: float):
@@ -589,6 +638,7 @@ def main():
     if args.only:
         fn = {"chunked": lambda: bench_chunked(W.C2, args.steps, args.warmup, peaks, flush, False),
               "decode": lambda: bench_decode(W.C3, args.steps, args.warmup, peaks, flush),
+              "pair": lambda: bench_pair_verify(args.steps, args.warmup, peaks, flush),
               "varlen": lambda: bench_varlen(W.C5, args.steps, args.warmup, peaks, flush),
               "yarn": lambda: bench_chunked(W.C4, args.steps, args.warmup, peaks, flush, False)}
         rec = fn[args.only]()
@@ -605,6 +655,7 @@ def main():
         dec_rec = bench_decode(W.C3, args.steps, args.warmup, peaks, flush)
         extra.append({k: v for k, v in dec_rec.items() if k != "importance"})
         extra.append(dec_rec["importance"])
+        extra.append(bench_pair_verify(args.steps, args.warmup, peaks, flush))
         extra.append(bench_varlen(W.C5, args.steps, args.warmup, peaks, flush))
         r4 = bench_chunked(W.C4, max(2, args.steps // 4), min(args.warmup, 3), peaks, flush,
                            with_e2e=False)

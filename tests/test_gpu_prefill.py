@@ -115,6 +115,27 @@ def test_prefill_window_long_history_splits(oracle):
     _compare_step(oracle, step, what="window + splits")
 
 
+SHORT_CHUNKS = {
+    # a speculative pair verify: two drafted tokens after a long history
+    "pair_verify_h32kv8": (W.Spec(H=32, KV=8, d=128, rd=128, rope=W.RopeParams(base=5e5)),
+                           [4093], [2], 4160),
+    "varlen_1_to_8_d64_gate": (W.Spec(H=8, KV=2, d=64, rd=64, out_gate=True),
+                               [0, 513, 77, 2000], [1, 8, 5, 3], 2048),
+    "window_softcap_qknorm": (W.Spec(H=10, KV=2, d=128, rd=64, qk_norm=True, window=300,
+                                     softcap=3.0), [1200, 5], [4, 7], 1280),
+}
+
+
+@pytest.mark.parametrize("name", list(SHORT_CHUNKS))
+def test_prefill_short_chunks(oracle, name):
+    """Chunks of a few new tokens (a speculative pair verify, drafted tokens):
+    the tile packs the group's query heads over the few tokens, so each K/V tile
+    is streamed once for all of them."""
+    spec, prior, new, cap = SHORT_CHUNKS[name]
+    step = W.make_step(spec, prior, new, cap, seed=79)
+    _compare_step(oracle, step, what=name)
+
+
 def test_prefill_varlen_small_all_rows(oracle):
     """Packed varlen step with qk-norm and gate (the mixed-serving options) at
     a size the oracle checks in full."""
