@@ -34,6 +34,7 @@ NA_QK_NORM = 1
 NA_QK_NORM_ZERO_CENTERED = 2
 NA_V_NORM = 4
 NA_OUT_GATE = 8
+NA_RING_CACHE = 16
 
 # Every symbol include/na.h declares.
 EXPORTED = ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
@@ -121,12 +122,14 @@ class AttnConfig:
     out_gate: bool = False
     softcap: float = 0.0
     window: int = 0
+    ring_cache: bool = False
 
     @property
     def flags(self) -> int:
         return ((NA_QK_NORM if self.qk_norm else 0)
                 | (NA_QK_NORM_ZERO_CENTERED if self.qk_norm_zero_centered else 0)
-                | (NA_V_NORM if self.v_norm else 0) | (NA_OUT_GATE if self.out_gate else 0))
+                | (NA_V_NORM if self.v_norm else 0) | (NA_OUT_GATE if self.out_gate else 0)
+                | (NA_RING_CACHE if self.ring_cache else 0))
 
     def c(self) -> na_attn_cfg:
         rd = self.head_dim if self.rotary_dim is None else self.rotary_dim

@@ -58,7 +58,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 __device__ __forceinline__ int attended_keys(const DecodeParams &p, int b, int &first)
 {
     const int n = __ldg(p.kv_lens + b);
-    if (n < 0 || n > p.capacity || n > p.max_kv_len) {
+    const bool ring = (p.flags & NA_RING_CACHE) != 0;  // positions wrap at the capacity
+    if (n < 0 || (!ring && n > p.capacity) || n > p.max_kv_len) {
         first = 0;
         return 0;
     }
@@ -274,10 +275,25 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
                 const int n = min(DEC_TILE, s1 - j0);
                 const uint32_t bytes = (uint32_t)(n * D * (int)sizeof(bf16));
                 mbar_arrive_expect_tx(&sm.full[stage], 2 * bytes);
-                bulk_copy_g2s(sm.k[stage], p.cache_k + head_base + (size_t)(pc.kf + j0) * D, bytes,
+                // Slot of the tile's first key; with a ring a tile that reaches the
+                // end of the slab continues at slot 0 (two copies, same stage).
+                int slot = pc.kf + j0;
+                int n1 = n;
+                if (p.flags & NA_RING_CACHE) {
+                    slot %= p.capacity;
+                    n1 = min(n, p.capacity - slot);
+                }
+                const uint32_t b1 = (uint32_t)(n1 * D * (int)sizeof(bf16));
+                bulk_copy_g2s(sm.k[stage], p.cache_k + head_base + (size_t)slot * D, b1,
                               &sm.full[stage], policy);
-                bulk_copy_g2s(sm.v[stage], p.cache_v + head_base + (size_t)(pc.kf + j0) * D, bytes,
+                bulk_copy_g2s(sm.v[stage], p.cache_v + head_base + (size_t)slot * D, b1,
                               &sm.full[stage], policy);
+                if (n1 < n) {
+                    bulk_copy_g2s(sm.k[stage] + (size_t)n1 * D, p.cache_k + head_base, bytes - b1,
+                                  &sm.full[stage], policy);
+                    bulk_copy_g2s(sm.v[stage] + (size_t)n1 * D, p.cache_v + head_base, bytes - b1,
+                                  &sm.full[stage], policy);
+                }
             }
         }
         // Let every copy this lane issued land before the CTA can exit.
@@ -536,7 +552,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     const int b = bh / p.H;
     const int n = __ldg(p.kv_lens + b);
     bf16 *out = p.out + (size_t)bh * D;
-    if (n < 0 || n > p.capacity || n > p.max_kv_len) {
+    if (n < 0 || (!(p.flags & NA_RING_CACHE) && n > p.capacity) || n > p.max_kv_len) {
         if (threadIdx.x == 0)
             na_report(p.status, NA_ERR_CAPACITY);
         for (int e = threadIdx.x; e < D; e += blockDim.x)

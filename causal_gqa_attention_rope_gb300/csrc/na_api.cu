@@ -10,7 +10,8 @@
 
 namespace {
 
-constexpr uint32_t kKnownFlags = NA_QK_NORM | NA_QK_NORM_ZERO_CENTERED | NA_V_NORM | NA_OUT_GATE;
+constexpr uint32_t kKnownFlags =
+    NA_QK_NORM | NA_QK_NORM_ZERO_CENTERED | NA_V_NORM | NA_OUT_GATE | NA_RING_CACHE;
 constexpr double kPi = 3.14159265358979323846;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -28,6 +29,8 @@ int check_cfg(const na_attn_cfg *c)
     if (!(c->rms_eps >= 0.f))
         return NA_ERR_INVALID_ARG;
     if (!(c->softcap >= 0.f) || !std::isfinite(c->softcap) || c->window < 0)
+        return NA_ERR_INVALID_ARG;
+    if ((c->flags & NA_RING_CACHE) && c->window <= 0)  // a ring only makes sense with a window
         return NA_ERR_INVALID_ARG;
     if (c->head_dim != 64 && c->head_dim != 128)
         return NA_ERR_UNSUPPORTED;
@@ -303,8 +306,15 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
         return NA_OK;
     if (!cu_seqlens || !cache_lens || !q_rot || !out || max_new_len <= 0)
         return NA_ERR_INVALID_ARG;
-    if (max_total_len > cache->capacity)
+    const bool ring = (cfg->flags & NA_RING_CACHE) != 0;
+    if (ring) {  // tiles of 128 keys never wrap; a whole chunk fits beside its rows' windows
+        if (cache->capacity % prefill_key_tile() != 0)
+            return NA_ERR_UNSUPPORTED;
+        if ((long long)cfg->window + max_new_len - 1 > cache->capacity)
+            return NA_ERR_CAPACITY;
+    } else if (max_total_len > cache->capacity) {
         return NA_ERR_CAPACITY;
+    }
     if ((long long)cache->batch * cfg->num_kv_heads * cache->capacity >= (1ll << 31) ||
         (long long)total_tokens * cfg->num_heads * cfg->head_dim >= (1ll << 40))
         return NA_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
@@ -409,7 +419,7 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
         return rc;
     if (!q_rot || !kv_lens || !out || !aligned16(q_rot) || !aligned16(out))
         return NA_ERR_INVALID_ARG;
-    if (max_kv_len > cache->capacity)
+    if ((cfg->flags & NA_RING_CACHE) ? cfg->window > cache->capacity : max_kv_len > cache->capacity)
         return NA_ERR_CAPACITY;
     if (probs && probs_stride < max_kv_len)
         return NA_ERR_CAPACITY;

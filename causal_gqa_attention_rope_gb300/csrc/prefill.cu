@@ -204,7 +204,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // start (0 without a window) to the last row; splits cut that range.
     const int win_tile = p.window > 0 ? max(0, pos_lo - p.window + 1) / BN * BN : 0;
     const int k_begin = win_tile + split_off;
-    const int row_base = (b * p.KV + kvh) * p.capacity + k_begin;
+    // Cache row of key tile j: with a ring the key position wraps at the
+    // capacity (a multiple of the key tile, so a tile never straddles the end).
+    const bool ring = (p.flags & NA_RING_CACHE) != 0;
+    const int kv_row0 = (b * p.KV + kvh) * p.capacity;
+    auto tile_row = [&](int j) {
+        const int k = k_begin + j * BN;
+        return kv_row0 + (ring ? k % p.capacity : k);
+    };
     int k_end = pos_hi + 1;
     if (p.num_splits > 1)
         k_end = min(k_end, k_begin + p.split_len);
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         run = false;
     } else if (r0 >= n_new) {
         run = false;
-    } else if (prior < 0 || pos_hi >= p.capacity || pos_hi >= p.max_total_len) {
+    } else if (prior < 0 || (!ring && pos_hi >= p.capacity) || pos_hi >= p.max_total_len) {
         if (threadIdx.x == 0)
             na_report(p.status, NA_ERR_CAPACITY);
         run = false;
@@ -257,10 +264,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = eager ? 1 : 0; j < pre; j++) {
             mbar_arrive_expect_tx(&sm.k_full[j], KB * BN * 128);
             for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_2d(sm.k[j][kb], &map_k, kb * 64, row_base + j * BN, &sm.k_full[j]);
+                tc::tma_load_2d(sm.k[j][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[j]);
             mbar_arrive_expect_tx(&sm.v_full[j], KB * BN * 128);
             for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_2d(sm.v[j][kb], &map_v, kb * 64, row_base + j * BN, &sm.v_full[j]);
+                tc::tma_load_2d(sm.v[j][kb], &map_v, kb * 64, tile_row(j), &sm.v_full[j]);
         }
     }
     tc::fence_before_sync();
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mbar_arrive_expect_tx(&sm.k_full[st], KB * BN * 128);
                 for (int kb = 0; kb < KB; kb++)
-                    tc::tma_load_2d(sm.k[st][kb], &map_k, kb * 64, row_base + j * BN, &sm.k_full[st]);
+                    tc::tma_load_2d(sm.k[st][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[st]);
                 if (!mbar_wait_bounded(&sm.v_empty[st], par) || aborted(&sm.abort_flag)) {
                     set_abort(&sm.abort_flag, p.status);
                     mbar_wait_bounded(&sm.k_full[st], (j / STAGES) & 1);
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mbar_arrive_expect_tx(&sm.v_full[st], KB * BN * 128);
                 for (int kb = 0; kb < KB; kb++)
-                    tc::tma_load_2d(sm.v[st][kb], &map_v, kb * 64, row_base + j * BN, &sm.v_full[st]);
+                    tc::tma_load_2d(sm.v[st][kb], &map_v, kb * 64, tile_row(j), &sm.v_full[st]);
                 issued = j + 1;
             }
             // every copy issued lands before the CTA can exit
@@ -678,7 +685,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
         if (m != FULL)
             break;
     }
-    if (pos < 0 || pos >= p.capacity || pos >= p.max_total_len)
+    if (pos < 0 || (!(p.flags & NA_RING_CACHE) && pos >= p.capacity) || pos >= p.max_total_len)
         return;  // reported by the split pass
     // Splits start at the key tile holding the window start of the row's query
     // tile (0 without a window), as in the split pass.

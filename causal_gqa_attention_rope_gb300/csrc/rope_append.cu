@@ -250,14 +250,14 @@ __device__ __forceinline__ const bf16 *row_src(const RopeAppendParams &p, int t,
     return p.v + ((size_t)t * p.KV + (r - p.H - p.KV)) * p.d;
 }
 
-__device__ __forceinline__ bf16 *row_dst(const RopeAppendParams &p, int t, int r, int b, int pos)
+__device__ __forceinline__ bf16 *row_dst(const RopeAppendParams &p, int t, int r, int b, int slot)
 {
     const size_t cap = (size_t)p.capacity;
     if (r < p.H)
         return p.q_out + ((size_t)t * p.H + r) * p.d;
     if (r < p.H + p.KV)
-        return p.cache_k + (((size_t)b * p.KV + (r - p.H)) * cap + pos) * p.d;
-    return p.cache_v + (((size_t)b * p.KV + (r - p.H - p.KV)) * cap + pos) * p.d;
+        return p.cache_k + (((size_t)b * p.KV + (r - p.H)) * cap + slot) * p.d;
+    return p.cache_v + (((size_t)b * p.KV + (r - p.H - p.KV)) * cap + slot) * p.d;
 }
 
 // Owner sequence b of token t (the last b with cu_seqlens[b] <= t, empty
@@ -361,11 +361,13 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
     }
     int b, pos;
     owner_of(p, t, lane, b, pos);
-    if (pos < 0 || pos >= p.capacity) {
+    const bool ring = (p.flags & NA_RING_CACHE) != 0;  // slot = pos % capacity
+    if (pos < 0 || (!ring && pos >= p.capacity)) {
         if (threadIdx.x == 0)
             na_report(p.status, NA_ERR_CAPACITY);
         return;
     }
+    const int slot = ring ? pos % p.capacity : pos;
     __syncthreads();
     if ((int)threadIdx.x < half)  // stored [i][k] for pair 8k + i: a row's lanes read adjacent entries
         cs[(threadIdx.x & 7) * 8 + (threadIdx.x >> 3)] = cos_sin_turns((unsigned)pos, fhi, flo, trig);
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
             }
         }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(row_dst(p, t, r, b, pos));
+    uint4 *dst = reinterpret_cast<uint4 *>(row_dst(p, t, r, b, slot));
     dst[e0 / 8] = f32_to_bf16x8(ya);
     dst[e1 / 8] = f32_to_bf16x8(yb);
 }
@@ -468,11 +470,13 @@ __global__ void __launch_bounds__(kStagedThreads) rope_append_staged_kernel(cons
     grid_dependents_launch();
     int b, pos;
     owner_of(p, t, lane, b, pos);
-    if (pos < 0 || pos >= p.capacity) {
+    const bool ring = (p.flags & NA_RING_CACHE) != 0;  // slot = pos % capacity
+    if (pos < 0 || (!ring && pos >= p.capacity)) {
         if (threadIdx.x == 0)
             na_report(p.status, NA_ERR_CAPACITY);
         return;
     }
+    const int slot = ring ? pos % p.capacity : pos;
     if (qk_norm) {
         for (int i = threadIdx.x; i < 2 * d; i += kStagedThreads)
             wq[i] = __bfloat162float(i < d ? p.qw[i] : p.kw[i - d]);
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kStagedThreads) rope_append_staged_kernel(cons
 
     for (int c = threadIdx.x; c < chunks; c += kStagedThreads) {
         const int r = c / cpr, j = c - r * cpr;
-        reinterpret_cast<uint4 *>(row_dst(p, t, r, b, pos))[j] = f32_to_bf16x8(xs + r * d + j * 8);
+        reinterpret_cast<uint4 *>(row_dst(p, t, r, b, slot))[j] = f32_to_bf16x8(xs + r * d + j * 8);
     }
 }
 

@@ -54,6 +54,15 @@ typedef enum na_status {
 #define NA_QK_NORM_ZERO_CENTERED 2u   /* with NA_QK_NORM: multiply by (1 + w) instead of w */
 #define NA_V_NORM 4u                  /* scale-less RMS of v before it enters the cache [cortiq fn vnorm_head] */
 #define NA_OUT_GATE 8u                /* out *= sigmoid(gate) after attention [cortiq fn apply_gate] */
+#define NA_RING_CACHE 16u             /* the cache is a ring: position pos lives in slot pos % capacity
+                                         (needle-core batch.rs, the per-position write-and-attend loop:
+                                         a ring of kv_window positions).  Needs window > 0.  The pages'
+                                         ring holds exactly the window, so writes and attends must
+                                         alternate; here the ring holds at least window + (new tokens
+                                         per sequence) - 1 positions, so a whole chunk is written first
+                                         without overwriting a key any of its rows still reads.
+                                         Prefill needs capacity % 128 == 0 and capacity >= window +
+                                         max_new_len - 1; decode needs capacity >= window. */
 
 /* One attention layer [cortiq struct QwenAttnCfg, the in-scope fields]. */
 typedef struct na_attn_cfg {

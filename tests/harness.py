@@ -273,3 +273,15 @@ def sample_rows(n: int, k: int, seed: int) -> List[int]:
     g = torch.Generator().manual_seed(seed)
     mid = torch.randperm(n - 2, generator=g)[:k] + 1
     return sorted(set([0, n - 1] + mid.tolist()))
+
+
+def ring_from_linear(cache: torch.Tensor, lens: Sequence[int], ring: int) -> torch.Tensor:
+    """A linear cache [B, KV, cap, d] laid out as a ring of `ring` slots per
+    (sequence, kv head): position p of the first lens[b] lives in slot p % ring
+    (only the last `ring` positions survive); untouched slots hold the sentinel."""
+    B, KV, _, d = cache.shape
+    out = W.sentinel_fill((B, KV, ring, d))
+    for b, n in enumerate(lens):
+        for pos in range(max(0, n - ring), n):
+            out[b, :, pos % ring] = cache[b, :, pos]
+    return out

@@ -56,6 +56,7 @@ def _cfg(**kw):
     (dict(softcap=float("nan")), na.NA_ERR_INVALID_ARG),
     (dict(softcap=float("inf")), na.NA_ERR_INVALID_ARG),
     (dict(window=-3), na.NA_ERR_INVALID_ARG),
+    (dict(ring_cache=True), na.NA_ERR_INVALID_ARG),  # a ring needs a window
 ])
 def test_bad_config_rejected_before_launch(lib, kw, code):
     c = _cfg(**kw)
@@ -153,3 +154,20 @@ def test_workspace_sizes_follow_the_plan(lib):
     assert ws % 16 == 0
     assert 64 * 32 * 130 * 4 <= ws <= 64 * 32 * 130 * 4 + 2 * 256 * 4 * 130 * 4 + 64 * 8 * 8
     assert na.na_decode_workspace_size(cfg, 128, 64) > ws
+
+
+def test_ring_cache_capacity_rules(lib):
+    """A ring cache needs whole 128-key tiles and room for a window plus a chunk
+    in prefill, and at least a window in decode (checked before any launch)."""
+    c = _cfg(window=200, ring_cache=True)
+    odd = na.na_kv_cache(16, 16, 1, 200)       # not a multiple of 128
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(c), 1, 16, 16, 10, 10, 5000, 16,
+                                   ctypes.byref(odd), None, 16, None, 1 << 30, None, None)
+    assert rc == na.NA_ERR_UNSUPPORTED
+    small = na.na_kv_cache(16, 16, 1, 128)     # window + 10 new - 1 > 128
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(c), 1, 16, 16, 10, 10, 5000, 16,
+                                   ctypes.byref(small), None, 16, None, 1 << 30, None, None)
+    assert rc == na.NA_ERR_CAPACITY
+    rc = lib.na_attn_decode(ctypes.byref(c), 1, 16, ctypes.byref(small), 16, 5000, None, 16,
+                            None, 0, 0, 16, 1 << 30, None, None)
+    assert rc == na.NA_ERR_CAPACITY            # window 200 > 128 slots

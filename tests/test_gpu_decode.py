@@ -78,6 +78,36 @@ def test_decode_softcap_and_window(oracle, name, spec):
     _check_importance(oracle, dec)
 
 
+def test_decode_ring_cache(oracle):
+    """Ring cache of 448 slots (not a multiple of the key tile) with a window of
+    300: key tiles that cross the end of the ring continue at slot 0."""
+    import causal_gqa_attention_rope_gb300 as na
+    from harness import attn_cfg, ring_from_linear
+    spec = W.Spec(H=8, KV=2, d=128, rd=128, window=300)
+    lens = [0, 1, 299, 300, 301, 700, 1500]
+    dec = W.make_decode(spec, lens, 1536, seed=107)
+    R = 448
+    dev = "cuda"
+    cfg = attn_cfg(spec)
+    cfg.ring_cache = True
+    cache = na.KVCache(ring_from_linear(dec.cache_k, lens, R).to(dev),
+                       ring_from_linear(dec.cache_v, lens, R).to(dev))
+    q = dec.q.to(dev)
+    out = torch.empty_like(q)
+    B, mx = len(lens), max(lens)
+    probs = torch.full((B, spec.H, mx), -7.0, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = na.workspace(na.na_decode_workspace_size(cfg, B, mx), dev)
+    na.na_attn_decode(cfg, q, cache, dec.kv_lens.to(dev), mx, out, probs=probs, workspace=ws,
+                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_out, ref_p = _oracle_decode(oracle, dec, stride=mx)
+    assert_out_close(out.cpu().double().numpy(), ref_out, "ring decode out")
+    for b, n in enumerate(lens):
+        assert_probs_close(probs[b, :, :n].cpu().numpy(), ref_p[b, :, :n], f"ring probs {b}")
+
+
 def test_decode_without_probs(oracle):
     dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128, out_gate=True), [300, 64], 512, seed=91)
     _check(oracle, dec, with_probs=False)

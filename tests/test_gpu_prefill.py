@@ -136,6 +136,52 @@ def test_prefill_short_chunks(oracle, name):
     _compare_step(oracle, step, what=name)
 
 
+def test_prefill_ring_cache(oracle):
+    """Ring cache (slot = position % capacity) with a window: the chunk is
+    appended into the ring, every row attends the last `window` keys, and the
+    ring holds exactly the newest `capacity` positions afterwards."""
+    import causal_gqa_attention_rope_gb300 as na
+    from harness import (attn_cfg, oracle_append, oracle_rows, ring_from_linear, rope_cfg,
+                         assert_within_ulp)
+    spec = W.Spec(H=8, KV=2, d=128, rd=128, window=200)
+    prior, new = [1000, 37, 0], [150, 5, 60]
+    step = W.make_step(spec, prior, new, 1300, seed=83)
+    R = 384  # a multiple of 128 and >= window + max new - 1
+    dev = "cuda"
+    cfg = attn_cfg(spec)
+    cfg.ring_cache = True
+    ck, cv = ring_from_linear(step.cache_k, prior, R), ring_from_linear(step.cache_v, prior, R)
+    cache = na.KVCache(ck.clone().to(dev), cv.clone().to(dev))
+    q, k, v = step.q.to(dev), step.k.to(dev), step.v.to(dev)
+    cu, lens = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
+    q_out, out = torch.empty_like(q), torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    T = step.total_tokens
+    max_new, max_tot = max(new), max(p + n for p, n in zip(prior, new))
+    na.na_rope_append_kv(cfg, rope_cfg(spec), cu, lens, q, k, v, q_out, cache, status=status)
+    ws = na.workspace(na.na_prefill_workspace_size(cfg, 3, T, max_new, max_tot), dev)
+    na.na_attn_prefill_chunk(cfg, cu, lens, max_new, max_tot, q_out, cache, out, workspace=ws,
+                             status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ost = oracle_append(oracle, step)
+    ref = oracle_rows(oracle, step, ost, list(range(T)))
+    assert_out_close(out.cpu().double().numpy(), ref, "ring prefill")
+    gk, gv = cache.k.cpu(), cache.v.cpu()
+    for b in range(3):
+        end = prior[b] + new[b]
+        for pos in range(max(0, end - R), end):
+            slot = pos % R
+            if pos >= prior[b]:  # appended now
+                assert_within_ulp(gk[b, :, slot], ost.cache_k[b, :, pos], f"ring K {b},{pos}")
+                assert np.array_equal(gv[b, :, slot].double().numpy(), ost.cache_v[b, :, pos])
+            else:  # history kept
+                assert torch.equal(gk[b, :, slot].view(torch.int16),
+                                   step.cache_k[b, :, pos].view(torch.int16))
+        for slot in range(end, R):  # never written
+            assert torch.equal(gk[b, :, slot].view(torch.int16), ck[b, :, slot].view(torch.int16))
+
+
 def test_prefill_varlen_small_all_rows(oracle):
     """Packed varlen step with qk-norm and gate (the mixed-serving options) at
     a size the oracle checks in full."""
