@@ -553,7 +553,7 @@ def bench_pair_verify(steps, warmup, peaks, flush):
     return {"workload": name, "metric": "pair verify KV GB/s", "unit": "GB/s", "value": ach,
             "ms_per_step": ms, "bytes_per_step": kv_bytes,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                         "frac": ach / peaks["hbm_gbs"], "traffic": traffic_from_profiles("prefill.cu", name),
                          "kernel": "na_attn_prefill_chunk (2-token chunks, GQA-packed tiles)",
                          "peak_source": peaks["source"] + " HBM copy"}}
 
