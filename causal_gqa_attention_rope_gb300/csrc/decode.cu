@@ -580,18 +580,61 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     const int ns = last - first + 1;
     const size_t row0 = (size_t)first * hpc + (r % hpc);
     const float *ml = p.part_ml + row0 * 2;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; s++)
+
+    // The first batch of this row's raw scores is requested before the merge
+    // arithmetic, so its latency overlaps the pieces' loads.
+    constexpr int PV = 8;  // 16-byte loads in flight per thread
+    constexpr int NT = 256;
+    // The row is walked as a scalar head up to its first 16-byte boundary,
+    // 16-byte groups of four keys, and a scalar tail (any stride).
+    float *pr = p.probs ? p.probs + (size_t)bh * p.probs_stride : nullptr;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(pr);
+    const int pre = (addr & 3) ? n : min(n, (int)(((16 - (addr & 15)) & 15) >> 2));
+    const int n4 = pr ? (n - pre) >> 2 : 0;
+    float4 *pr4 = reinterpret_cast<float4 *>(pr + pre);
+    float4 x[PV];
+#pragma unroll
+    for (int u = 0; u < PV; u++) {
+        const int i = threadIdx.x + u * NT;
+        if (i < n4)
+            x[u] = pr4[i];
+    }
+
+    // Row maximum and sum over the pieces: every warp reduces them, its lanes
+    // taking the pieces lane, lane + 32, ... (a fixed order: the same sum on
+    // every run).
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    float m0 = -INFINITY, l0 = 0.f;
+    if (lane < ns) {
+        m0 = ml[2 * hpc * lane];
+        l0 = ml[2 * hpc * lane + 1];
+    }
+    float M = m0;
+    for (int s = lane + 32; s < ns; s += 32)
         M = fmaxf(M, ml[2 * hpc * s]);
-    float L = 0.f;
-    for (int s = 0; s < ns; s++)
-        L += ml[2 * hpc * s + 1] * exp2f(ml[2 * hpc * s] - M);
-    const float inv_l = 1.0f / L;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    float L = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - M);
+    for (int s = lane + 32; s < ns; s += 32) {
+        const float m = ml[2 * hpc * s];
+        if (m != -INFINITY)
+            L += ml[2 * hpc * s + 1] * exp2f(m - M);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        L += __shfl_xor_sync(FULL, L, o);
+    const float inv_l = L > 0.f ? 1.0f / L : 0.f;
+
     const float *po = p.part_o + row0 * D;
-    for (int e = threadIdx.x; e < D; e += blockDim.x) {
+    for (int e = threadIdx.x; e < D; e += NT) {
         float o = 0.f;
-        for (int s = 0; s < ns; s++)
-            o += po[(size_t)s * hpc * D + e] * exp2f(ml[2 * hpc * s] - M);
+        for (int s = 0; s < ns; s++) {
+            const float m = ml[2 * hpc * s];
+            if (m != -INFINITY)
+                o += po[(size_t)s * hpc * D + e] * exp2f(m - M);
+        }
         o *= inv_l;
         if ((p.flags & NA_OUT_GATE) && p.gate) {
             const float g = __bfloat162float(p.gate[(size_t)bh * D + e]);
@@ -599,28 +642,37 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
         }
         out[e] = __float2bfloat16_rn(o);
     }
-    if (p.probs) {
+    if (pr) {
         // keys before the window (none without one) get probability 0
         const int kf = (p.window > 0 && n > p.window) ? n - p.window : 0;
-        float *pr = p.probs + (size_t)bh * p.probs_stride;
         auto prob = [&](float raw, int j) { return j < kf ? 0.f : exp2f(raw - M) * inv_l; };
-        if ((p.probs_stride & 3) == 0) {
-            const int n4 = n >> 2;
-            float4 *pr4 = reinterpret_cast<float4 *>(pr);
-            for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-                float4 x = pr4[i];
-                x.x = prob(x.x, 4 * i);
-                x.y = prob(x.y, 4 * i + 1);
-                x.z = prob(x.z, 4 * i + 2);
-                x.w = prob(x.w, 4 * i + 3);
-                pr4[i] = x;
+        for (int base = 0; base < n4; base += PV * NT) {
+            if (base > 0) {
+#pragma unroll
+                for (int u = 0; u < PV; u++) {
+                    const int i = base + threadIdx.x + u * NT;
+                    if (i < n4)
+                        x[u] = pr4[i];
+                }
             }
-            for (int j = (n4 << 2) + threadIdx.x; j < n; j += blockDim.x)
-                pr[j] = prob(pr[j], j);
-        } else {
-            for (int j = threadIdx.x; j < n; j += blockDim.x)
-                pr[j] = prob(pr[j], j);
+#pragma unroll
+            for (int u = 0; u < PV; u++) {
+                const int i = base + threadIdx.x + u * NT;
+                if (i < n4) {
+                    const int j = pre + 4 * i;
+                    float4 y = x[u];
+                    y.x = prob(y.x, j);
+                    y.y = prob(y.y, j + 1);
+                    y.z = prob(y.z, j + 2);
+                    y.w = prob(y.w, j + 3);
+                    pr4[i] = y;
+                }
+            }
         }
+        for (int j = threadIdx.x; j < pre; j += NT)
+            pr[j] = prob(pr[j], j);
+        for (int j = pre + (n4 << 2) + threadIdx.x; j < n; j += NT)
+            pr[j] = prob(pr[j], j);
     }
 }
 

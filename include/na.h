@@ -229,7 +229,10 @@ int na_attn_decode_static_ws(const na_attn_cfg *cfg, int32_t batch, const void *
  *
  *   imp[b][j] = sum over the H query heads of probs[b][h][j]     for j < kv_lens[b]
  * or, with accumulate != 0, imp[b][j] += that sum.  Keys past kv_lens[b] are not
- * touched.  The sum runs over heads in index order in fp32 (deterministic).
+ * touched.  The sum is fp32 and deterministic: the heads are cut into four
+ * consecutive groups, each summed in index order, and the group sums are added
+ * in group order.  Both strides a multiple of 4 with 16-byte-aligned probs and
+ * imp give 16-byte accesses (the fast layout); any stride is correct.
  *
  *   probs       fp32 [batch][H][probs_stride]: the probabilities na_attn_decode wrote.
  *   kv_lens     int32 [batch] (device), the same lengths given to na_attn_decode.

@@ -197,6 +197,30 @@ def test_decode_importance(oracle, stride):
     _check_importance(oracle, dec, probs_stride=stride)
 
 
+@pytest.mark.parametrize("H,stride", [(5, 1028), (3, 1031), (40, 1028)])
+def test_importance_head_counts(oracle, H, stride):
+    """Importance alone, on given probabilities: head counts that do not split
+    evenly over the kernel's thread groups, ragged lengths around its 256-key
+    blocks, a scalar-path stride (not a multiple of 4) and accumulation."""
+    gen = torch.Generator().manual_seed(H)
+    lens = torch.tensor([0, 1, 255, 256, 257, 1027], dtype=torch.int32)
+    B = lens.numel()
+    probs = torch.rand((B, H, stride), generator=gen, dtype=torch.float32)
+    init = torch.rand((B, stride), generator=gen, dtype=torch.float32)
+    dec = W.DecodeInputs(spec=W.Spec(H=H, KV=1, d=64, rd=64), q=None, cache_k=None,
+                         cache_v=None, kv_lens=lens, gate=None)
+    got, st = _gpu_importance(dec, probs, init, True)
+    assert st == 0
+    ref = oracle.decode_importance(H, probs.double().numpy(), lens.numpy(),
+                                   imp=init.double().numpy(), accumulate=True)
+    for b, n in enumerate(lens.tolist()):
+        # H fp32 additions of terms in [0, 1) (the start value included): in any
+        # order the rounding error is at most H * 2^-24 * (H + 1)
+        err = float(np.max(np.abs(got[b, :n].double().numpy() - ref[b, :n]))) if n else 0.0
+        assert err <= H * (H + 1) * 2.0 ** -24, f"importance b{b}: {err:.3e}"
+        assert torch.equal(got[b, n:], init[b, n:]), "importance written past kv_len"
+
+
 def test_decode_importance_accumulates(oracle):
     dec = W.make_decode(W.Spec(H=16, KV=2, d=64, rd=64), [5, 64, 333], 512, seed=98)
     _check_importance(oracle, dec, accumulate=True)
@@ -223,3 +247,22 @@ def test_full_decode_importance_b64_h32kv8(oracle):
         n = lens[b]
         err = float(np.max(np.abs(got[b, :n].double().numpy() - ref[0, :n])))
         assert err <= H * PROBS_MAX_ABS, f"importance b{b}: {err:.3e}"
+
+
+def test_calls_follow_the_current_stream(oracle):
+    """With no stream argument the binding launches on the current stream, also
+    inside a `torch.cuda.stream` block; the result is the same as on the default
+    stream."""
+    import causal_gqa_attention_rope_gb300 as na
+    assert na._stream(None) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert na._stream(None) == side.cuda_stream
+    dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128), [300, 77], capacity=320, seed=5)
+    ref_out, _ = gpu_decode(dec, with_probs=False)[:2]
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        out, _, status = gpu_decode(dec, with_probs=False)
+    torch.cuda.synchronize()
+    assert status == 0
+    assert torch.equal(out, ref_out)
