@@ -680,18 +680,18 @@ template <int D, int HPC, bool CAPPED>
 cudaError_t launch_split(const DecodeParams &p, cudaStream_t stream)
 {
     const size_t smem = sizeof(DecSmem<D, HPC>);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, HPC, CAPPED>,
+    static std::atomic<unsigned long long> configured{0};
+    const cudaError_t e = once_per_device(configured, [smem] {
+        cudaError_t r = cudaFuncSetAttribute(decode_split_kernel<D, HPC, CAPPED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_split_kernel<D, HPC, CAPPED>,
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(decode_split_kernel<D, HPC, CAPPED>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+        return r;
+    });
+    if (e != cudaSuccess)
+        return e;
     return launch_kernel(decode_split_kernel<D, HPC, CAPPED>, dim3(p.grid), dim3(DEC_THREADS), smem,
                          stream, p);
 }

@@ -54,16 +54,22 @@ int check_cache(const na_kv_cache *cache, int batch)
 
 int sm_count()
 {
-    static int cached = 0;
-    if (cached == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-            cached = n;
-        else
-            return 148;
+    // per device; an unreadable count plans for 152 SMs (the launches then
+    // report the device error themselves)
+    static std::atomic<int> cached[kMaxDevices];
+    const int dev = current_device_index();
+    if (dev >= 0) {
+        const int n = cached[dev].load(std::memory_order_relaxed);
+        if (n > 0)
+            return n;
     }
-    return cached;
+    int d = 0, n = 0;
+    if (cudaGetDevice(&d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0)
+        return 152;
+    if (dev >= 0)
+        cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 // RoPE inverse frequencies in double (cortiq fns rope_inv_freq / yarn_inv_freq,

@@ -2,6 +2,7 @@
 // kernels of the attention library (sm_103a).
 #pragma once
 
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -187,6 +188,33 @@ cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Host setup that must run once per device (kernel attributes): `setup`
+// (returning cudaError_t, idempotent) runs unless it already succeeded on the
+// calling thread's current device.  Threads racing on a first call may both run
+// it; the per-device bit is published only after a success.
+constexpr int kMaxDevices = 64;
+
+inline int current_device_index()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return -1;  // not cached: the setup runs every time
+    return dev;
+}
+
+template <typename F>
+cudaError_t once_per_device(std::atomic<unsigned long long> &done, F &&setup)
+{
+    const int dev = current_device_index();
+    const unsigned long long bit = dev >= 0 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    const cudaError_t e = setup();
+    if (e == cudaSuccess && bit)
+        done.fetch_or(bit, std::memory_order_release);
+    return e;
 }
 
 // ------------------------------------------------------ launch parameters --

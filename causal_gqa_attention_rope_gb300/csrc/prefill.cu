@@ -845,21 +845,20 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
             return cudaErrorInvalidValue;
     }
     const size_t smem = tc_smem_bytes<D>();
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, false>,
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = once_per_device(configured, [smem] {
+        cudaError_t r = cudaFuncSetAttribute(prefill_tc_kernel<D, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_tc_kernel<D, true>,
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_tc_kernel<D, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+        return r;
+    });
+    if (e != cudaSuccess)
+        return e;
     dim3 grid(p.q_tiles, p.H / p.pack, p.batch * p.num_splits);
-    cudaError_t e = p.softcap > 0.f
-                        ? launch_kernel(prefill_tc_kernel<D, true>, grid, dim3(THREADS), smem, stream,
-                                        p, mq, mk, mv)
+    e = p.softcap > 0.f ? launch_kernel(prefill_tc_kernel<D, true>, grid, dim3(THREADS), smem,
+                                        stream, p, mq, mk, mv)
                         : launch_kernel(prefill_tc_kernel<D, false>, grid, dim3(THREADS), smem,
                                         stream, p, mq, mk, mv);
     if (e != cudaSuccess || p.num_splits == 1)

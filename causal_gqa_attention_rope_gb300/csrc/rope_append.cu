@@ -595,14 +595,20 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq
                              p, turns);
     }
     const size_t smem = rope_append_smem_bytes(p.H, p.KV, p.d, p.rd);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
+    // the largest dynamic shared memory granted so far, per device
+    static std::atomic<size_t> configured[kMaxDevices];
+    const int dev = current_device_index();
+    if (smem > 48 * 1024 && (dev < 0 || smem > configured[dev].load(std::memory_order_acquire))) {
         cudaError_t e = cudaFuncSetAttribute(rope_append_staged_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess)
             return e;
-        configured = smem;
+        if (dev >= 0) {
+            size_t cur = configured[dev].load(std::memory_order_relaxed);
+            while (cur < smem && !configured[dev].compare_exchange_weak(cur, smem))
+                ;
+        }
     }
     return launch_kernel(rope_append_staged_kernel, dim3(p.total_tokens), dim3(kStagedThreads), smem,
                          stream, p, turns);
