@@ -494,6 +494,47 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
     assert int(status.item()) == 0
     ims = statistics.mean(it)
     iach = imp_bytes / (ims * 1e-3) / 1e9
+    # The same decode with the importance summed in its merge pass (one call):
+    # the K/V, the probabilities once (written) and the running importance
+    # (read and written) per step.
+    def run_fused(ev=None):
+        na.na_rope_append_kv(cfg, rope, cu, prior, q_new, k_new, v_new, q_rot, cache,
+                             status=status)
+        if ev:
+            ev[0].record()
+        na.na_attn_decode_imp(cfg, q_rot, cache, kv_lens, max_kv, out, probs, imp,
+                              accumulate=True, workspace=ws, status=status)
+        if ev:
+            ev[1].record()
+
+    for _ in range(warmup):
+        run_fused()
+    torch.cuda.synchronize()
+    ft, fk = [], []
+    for _ in range(steps):
+        flush()
+        torch.cuda._sleep(5_000_000)
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run_fused(ev)
+        b.record()
+        torch.cuda.synchronize()
+        ft.append(a.elapsed_time(b))
+        fk.append(ev[0].elapsed_time(ev[1]))
+    assert int(status.item()) == 0
+    fms, fkms = statistics.mean(ft), statistics.mean(fk)
+    fused_bytes = alg_bytes + sum(lens) * 2 * 4
+    fach = fused_bytes / (fkms * 1e-3) / 1e9
+    fused = {"workload": "decode_imp_" + wl.name, "metric": "decode+importance KV GB/s",
+             "unit": "GB/s", "value": (fused_bytes + B * 3 * KV * d * 2) / (fms * 1e-3) / 1e9,
+             "ms_per_step": fms, "bytes_per_step": fused_bytes,
+             "roofline": {"bound": "hbm", "achieved": fach, "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": fach / peaks["hbm_gbs"],
+                          "traffic": traffic_from_profiles("decode.cu", "decode_imp_" + wl.name),
+                          "kernel": "na_attn_decode_imp (split pass + merge pass with importance)",
+                          "peak_source": peaks["source"] + " HBM copy"}}
+
     importance = {"workload": "importance_" + wl.name, "metric": "importance GB/s", "unit": "GB/s",
                   "value": iach, "ms_per_step": ims, "bytes_per_step": imp_bytes,
                   "roofline": {"bound": "hbm", "achieved": iach, "peak": peaks["hbm_gbs"],
@@ -510,7 +551,7 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
                          "traffic": traffic_from_profiles("decode.cu", wl.name),
                          "kernel": "na_attn_decode (split pass + combine)",
                          "peak_source": peaks["source"] + " HBM copy"},
-            "importance": importance}
+            "importance": importance, "fused": fused}
 
 
 def bench_pair_verify(steps, warmup, peaks, flush):
@@ -657,8 +698,9 @@ def main():
     extra = []
     if not args.no_extra:
         dec_rec = bench_decode(W.C3, args.steps, args.warmup, peaks, flush)
-        extra.append({k: v for k, v in dec_rec.items() if k != "importance"})
+        extra.append({k: v for k, v in dec_rec.items() if k not in ("importance", "fused")})
         extra.append(dec_rec["importance"])
+        extra.append(dec_rec["fused"])
         extra.append(bench_pair_verify(args.steps, args.warmup, peaks, flush))
         extra.append(bench_varlen(W.C5, args.steps, args.warmup, peaks, flush))
         r4 = bench_chunked(W.C4, max(2, args.steps // 4), min(args.warmup, 3), peaks, flush,
