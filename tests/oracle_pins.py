@@ -333,8 +333,8 @@ def pin_chunked_equals_single_chunk(o):
 
 
 def pin_decode_equals_last_prefill_row(o):
-    """Decode of the token at position p equals the prefill row at p; a
-    two-token chunk equals two decode steps (append then attend)."""
+    """Decode of the token at position p equals the prefill row at p of the
+    whole prompt (append then attend)."""
     rng = np.random.default_rng(9)
     H, KV, d, L = 4, 2, 8, 7
     inv = o.rope_inv_freq(d, 10000.0)
@@ -348,6 +348,39 @@ def pin_decode_equals_last_prefill_row(o):
         dec, _ = o.decode(H, KV, d, 0.3, 0, q_rot[p].reshape(1, H, d), ck, cv, [p + 1],
                           want_probs=False)
         _close(dec[0], out[p], 1e-14, f"decode at {p}")
+
+
+def pin_pair_chunk_equals_two_decode_steps(o):
+    """A speculative pair verify: a two-token chunk over a filled cache gives
+    the rows of two decode steps, each appending its token and then attending
+    (cortiq qwen_attention_batch attends a batch of positions of one sequence;
+    its decode path appends, then attends).  Plain, with a sliding window and
+    with a soft cap; the two caches agree bit for bit."""
+    rng = np.random.default_rng(21)
+    H, KV, d, P = 4, 2, 8, 6
+    inv = o.rope_inv_freq(d, 10000.0)
+    scale = 0.3
+    q = rng.standard_normal((P + 2, H, d))
+    k = rng.standard_normal((P + 2, KV, d))
+    v = rng.standard_normal((P + 2, KV, d))
+    for softcap, window in ((0.0, 0), (0.0, 3), (2.5, 0)):
+        ck1, cv1 = np.zeros((1, KV, P + 2, d)), np.zeros((1, KV, P + 2, d))
+        o.rope_append(H, KV, d, d, 0, 1e-6, inv, 1.0, [0, P], [0], q[:P], k[:P], v[:P], None,
+                      None, ck1, cv1)
+        ck2, cv2 = ck1.copy(), cv1.copy()
+        q_rot = o.rope_append(H, KV, d, d, 0, 1e-6, inv, 1.0, [0, 2], [P], q[P:], k[P:], v[P:],
+                              None, None, ck1, cv1)
+        pair = o.attend_rows(H, KV, d, scale, 0, [0, 2], [P], q_rot, ck1, cv1, None, [0, 1],
+                             softcap=softcap, window=window)
+        for t in range(2):
+            s = slice(P + t, P + t + 1)
+            qt = o.rope_append(H, KV, d, d, 0, 1e-6, inv, 1.0, [0, 1], [P + t], q[s], k[s], v[s],
+                               None, None, ck2, cv2)
+            dec, _ = o.decode(H, KV, d, scale, 0, qt.reshape(1, H, d), ck2, cv2, [P + t + 1],
+                              want_probs=False, softcap=softcap, window=window)
+            _close(dec[0], pair[t], 1e-14, f"pair row {t} (cap {softcap}, window {window})")
+        _close(ck1, ck2, 0.0, "cache k")
+        _close(cv1, cv2, 0.0, "cache v")
 
 
 def pin_gate_values(o):
