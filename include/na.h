@@ -12,7 +12,8 @@
  *     (varlen packing): token t belongs to sequence b when
  *     cu_seqlens[b] <= t < cu_seqlens[b+1].
  *   - The KV cache is head-major, one slot per absolute position:
- *     k[b][kv_head][slot][head_dim] (same for v), slot = position.
+ *     k[b][kv_head][slot][head_dim] (same for v), slot = position
+ *     (position % capacity with NA_RING_CACHE).
  *   - Every pointer argument is DEVICE memory unless its comment says HOST.
  *     Configuration structs are HOST memory and are read only during the call.
  *   - Ownership: the caller allocates and frees every buffer (including the
@@ -110,6 +111,7 @@ typedef struct na_kv_cache {
  *   q_out[t][h]            = RoPE(norm_q(q[t][h]), pos)         for every h
  *   cache.k[b][g][pos]     = RoPE(norm_k(k[t][g]), pos)         for every g
  *   cache.v[b][g][pos]     = vnorm(v[t][g])  (or v unchanged)
+ * (slot pos % capacity instead of pos with NA_RING_CACHE).
  * RoPE turns pairs (x[i], x[i + rd/2]), i < rd/2, by pos * inv_freq[i] and
  * multiplies both outputs by the attention factor.
  *
@@ -142,12 +144,17 @@ int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_
  * New token t of sequence b at pos = cache_lens[b] + (t - cu_seqlens[b]) and
  * query head h attends keys 0 .. pos of kv head h / (H / KV):
  *   out[t][h] = sum_j softmax_j(scale * q_rot[t][h] . k_j) v_j   (* sigmoid(gate[t][h]))
+ * With cfg->window > 0 only keys pos - window + 1 .. pos are attended; with
+ * cfg->softcap > 0 each scaled score is capped before the softmax.  Chunks of a
+ * few tokens per sequence (the drafted tokens of a speculative verify) are
+ * valid chunks: each attends the cache plus its own earlier tokens.
  *
  *   cu_seqlens    int32 [batch + 1], non-decreasing, cu_seqlens[0] == 0.
  *   cache_lens    int32 [batch]: prior lengths (the same values given to na_rope_append_kv).
  *   total_tokens  HOST copy of cu_seqlens[batch]; 0 is a no-op returning NA_OK.
  *   max_new_len   HOST upper bound of cu_seqlens[b+1] - cu_seqlens[b].
- *   max_total_len HOST upper bound of cache_lens[b] + new length; <= capacity.
+ *   max_total_len HOST upper bound of cache_lens[b] + new length; <= capacity unless
+ *                 NA_RING_CACHE (then positions wrap; see that flag for its capacity rules).
  *   q_rot         bf16 [total_tokens][H][d] (q_out of na_rope_append_kv).
  *   gate          bf16 [total_tokens][H][d], required with NA_OUT_GATE, else ignored.
  *   out           bf16 [total_tokens][H][d].
