@@ -40,7 +40,8 @@ NA_RING_CACHE = 16
 # Every symbol include/na.h declares.
 EXPORTED = ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
             "na_attn_decode_static_ws", "na_decode_importance", "na_attn_decode_imp",
-            "na_prefill_workspace_size", "na_decode_workspace_size", "na_status_string")
+            "na_prefill_workspace_size", "na_decode_workspace_size", "na_status_string",
+            "na_selftest_wait_timeout")
 
 
 class na_attn_cfg(ctypes.Structure):
@@ -95,11 +96,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                        I32, P, SZ, P, P]
     lib.na_prefill_workspace_size.argtypes = [cfgp, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_decode_workspace_size.argtypes = [cfgp, I32, I32, I32, ctypes.POINTER(SZ)]
+    lib.na_selftest_wait_timeout.argtypes = [P, P]
     lib.na_status_string.argtypes = [ctypes.c_int]
     lib.na_status_string.restype = ctypes.c_char_p
     for name in ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
                  "na_attn_decode_static_ws", "na_decode_importance", "na_attn_decode_imp",
-                 "na_prefill_workspace_size", "na_decode_workspace_size"):
+                 "na_prefill_workspace_size", "na_decode_workspace_size",
+                 "na_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -314,6 +317,13 @@ def na_decode_importance(cfg: AttnConfig, probs, kv_lens, max_kv_len: int, imp,
                                   int(imp.shape[-1]), 1 if accumulate else 0, _ptr(status),
                                   _stream(stream))
     _check("na_decode_importance", rc)
+
+
+def na_selftest_wait_timeout(status, stream=None):
+    """Run the library's bounded device wait on a barrier nothing completes:
+    after about a second `status` holds NA_ERR_DEVICE_TIMEOUT."""
+    _check("na_selftest_wait_timeout",
+           load_library().na_selftest_wait_timeout(_ptr(status), _stream(stream)))
 
 
 def workspace(nbytes: int, device="cuda"):

@@ -23,7 +23,6 @@ static __device__ __align__(256) unsigned char g_decode_scratch[NA_STATIC_DECODE
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_lock;
 void *g_scratch_ptr[kMaxDevices];
 

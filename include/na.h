@@ -292,6 +292,20 @@ int na_prefill_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t tot
 int na_decode_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t max_kv_len,
                              int32_t num_splits, size_t *bytes);
 
+/*
+ * Self-test of the device-side failure detection (an addition of this
+ * library).  Every wait inside the library's kernels gives up after about a
+ * second (2^31 SM cycles) and writes NA_ERR_DEVICE_TIMEOUT into the caller's
+ * status word instead of hanging.  This call runs that same bounded wait, in a
+ * one-CTA kernel, on a barrier that nothing ever completes: after about a
+ * second *status holds NA_ERR_DEVICE_TIMEOUT (unless it already held an error),
+ * the kernel returns normally and the context stays usable.
+ *
+ *   status  device int32, required.
+ * Errors: NA_ERR_INVALID_ARG for a NULL status; NA_ERR_CUDA if the launch fails.
+ */
+int na_selftest_wait_timeout(int32_t *status, void *stream);
+
 /* Static description of a status code (HOST string, never NULL). */
 const char *na_status_string(int status);
 

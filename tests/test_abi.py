@@ -126,6 +126,10 @@ def test_decode_with_importance_validated(lib):
     assert call(c, 16, 64, 16, 64, ws_bytes=8) == na.NA_ERR_WORKSPACE
 
 
+def test_wait_selftest_needs_a_status_word(lib):
+    assert lib.na_selftest_wait_timeout(None, None) == na.NA_ERR_INVALID_ARG
+
+
 def test_rope_params_validated(lib):
     c = _cfg()
     cache = na.na_kv_cache(16, 16, 1, 64)
