@@ -191,3 +191,22 @@ def test_ring_cache_capacity_rules(lib):
     rc = lib.na_attn_decode(ctypes.byref(c), 1, 16, ctypes.byref(small), 16, 5000, None, 16,
                             None, 0, 0, 16, 1 << 30, None, None)
     assert rc == na.NA_ERR_CAPACITY            # window 200 > 128 slots
+
+
+def test_no_fallback_without_the_library(tmp_path, monkeypatch):
+    """A missing libna.so raises instead of falling back to any other path."""
+    monkeypatch.setattr(na, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        na.load_library(str(tmp_path / "libna.so"))
+
+
+def test_no_fallback_for_cpu_tensors(lib):
+    """Compute calls take CUDA tensors only: CPU tensors raise before any launch."""
+    import torch
+    cfg = na.AttnConfig(4, 2, 64)
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    cache = na.KVCache(torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16),
+                       torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16))
+    kv = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        na.na_attn_decode(cfg, q, cache, kv, 1, torch.empty_like(q))
