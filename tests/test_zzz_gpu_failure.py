@@ -1,6 +1,7 @@
 """Device-side failure detection without a GPU fault: a bounded wait that runs
 out reports NA_ERR_DEVICE_TIMEOUT in the caller's status word, the kernel
-returns, and the context keeps working."""
+returns, and the context keeps working.  This file runs last so that a failure
+here leaves every other test already run."""
 import time
 
 import pytest
