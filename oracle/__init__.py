@@ -11,7 +11,7 @@ Pages it follows (docs.rs source pages): cortiq-engine 0.5.39
 ``rope_rotate_scaled``, ``rmsnorm_head``, ``vnorm_head``, ``attention_head``,
 ``apply_gate``, ``qwen_attention_batch``) and needle-core 0.3.1
 ``src/v2/batch.rs`` (module doc "What has to stay sequential",
-fn ``batch_attention``).
+fn ``batch_attention`` and its ring of ``kv_window`` positions).
 """
 from __future__ import annotations
 
@@ -32,6 +32,7 @@ QK_NORM = 1
 QK_NORM_ZERO_CENTERED = 2
 V_NORM = 4
 OUT_GATE = 8
+RING_CACHE = 16
 
 
 def compile_oracle(source: str = SOURCE, out_path: str = LIB_PATH) -> str:
@@ -100,7 +101,14 @@ class Oracle:
         lib.oracle_decode_importance.argtypes = [ctypes.c_int, ctypes.c_int, _D, ctypes.c_int, _I,
                                                  _D, ctypes.c_int, ctypes.c_int]
         lib.oracle_decode_importance.restype = None
+        lib.oracle_ring_slot.argtypes = [ctypes.c_int64, ctypes.c_int]
+        lib.oracle_ring_slot.restype = ctypes.c_int
         self.lib = lib
+
+    # --- cache layout ---
+    def ring_slot(self, pos: int, capacity: int) -> int:
+        """Slot of position ``pos`` in a ring cache of ``capacity`` slots."""
+        return int(self.lib.oracle_ring_slot(int(pos), int(capacity)))
 
     # --- RoPE frequencies (cortiq fns rope_inv_freq / yarn_inv_freq) ---
     def rope_inv_freq(self, rd: int, base: float) -> np.ndarray:

@@ -29,6 +29,9 @@
  *   - sigmoid output gate:            cortiq, fn apply_gate
  *   - decode with per-key probs:      cortiq, fn attention_head (returned probs),
  *                                     fn qwen_attention_core (append then attend)
+ *   - ring cache (slot = pos mod cap): needle, fn batch_attention (the
+ *                                     per-position write-and-attend loop over a
+ *                                     ring of kv_window positions)
  *
  * Readings where the pages leave a choice (each one is listed with its reason
  * in the design notes of this repository):
@@ -51,6 +54,7 @@
 #define ORACLE_QK_NORM_ZERO_CENTERED 2
 #define ORACLE_V_NORM 4
 #define ORACLE_OUT_GATE 8
+#define ORACLE_RING_CACHE 16
 
 /* ---------------------------------------------------------------- RoPE --- */
 
@@ -177,13 +181,28 @@ static size_t cache_index(int b, int kvh, int slot, int KV, int capacity, int d)
     return (((size_t)b * KV + kvh) * (size_t)capacity + (size_t)slot) * (size_t)d;
 }
 
+/* Ring cache (needle fn batch_attention: the cache of a windowed layer is a
+ * ring that each new position overwrites in turn): position pos lives in slot
+ * pos mod capacity, so the ring holds the newest `capacity` positions. */
+int oracle_ring_slot(int64_t pos, int capacity)
+{
+    return (int)(pos % (int64_t)capacity);
+}
+
+/* Slot of position pos: the position itself, or its ring slot. */
+static int slot_of(int flags, int64_t pos, int capacity)
+{
+    return (flags & ORACLE_RING_CACHE) ? oracle_ring_slot(pos, capacity) : (int)pos;
+}
+
 /* Per new token (cortiq fn finish_projection, then cache append):
  *   pos = cache_lens[b] + (t - cu_seqlens[b]);
  *   q, k: optional per-head RMSNorm, then RoPE on the first rd dims;
  *   v: optional scale-less V-norm;
- *   q_out[t] <- q;  cache_k[b][kvh][pos] <- k;  cache_v[b][kvh][pos] <- v.
+ *   q_out[t] <- q;  cache_k[b][kvh][slot] <- k;  cache_v[b][kvh][slot] <- v,
+ * slot = pos, or pos mod capacity with a ring cache (ORACLE_RING_CACHE).
  * Tensors: q, q_out [T][H][d]; k, v [T][KV][d]; caches [B][KV][capacity][d].
- * Returns 0, or -1 when a position does not fit the capacity (nothing past
+ * Returns 0, or -1 when a position does not fit a linear cache (nothing past
  * that token is written). */
 int oracle_rope_append(int H, int KV, int d, int rd, int flags, double eps,
                        const double *inv_freq, double rope_scale, int batch,
@@ -196,8 +215,9 @@ int oracle_rope_append(int H, int KV, int d, int rd, int flags, double eps,
     for (int b = 0; b < batch; b++) {
         for (int t = cu_seqlens[b]; t < cu_seqlens[b + 1]; t++) {
             int pos = cache_lens[b] + (t - cu_seqlens[b]);
-            if (pos < 0 || pos >= capacity)
+            if (pos < 0 || (!(flags & ORACLE_RING_CACHE) && pos >= capacity))
                 return -1;
+            int slot = slot_of(flags, pos, capacity);
             for (int h = 0; h < H; h++) {
                 double *x = q_out + ((size_t)t * H + h) * d;
                 for (int i = 0; i < d; i++)
@@ -207,8 +227,8 @@ int oracle_rope_append(int H, int KV, int d, int rd, int flags, double eps,
                 oracle_rope_rotate(x, rd, pos, inv_freq, rope_scale);
             }
             for (int g = 0; g < KV; g++) {
-                double *kx = cache_k + cache_index(b, g, pos, KV, capacity, d);
-                double *vx = cache_v + cache_index(b, g, pos, KV, capacity, d);
+                double *kx = cache_k + cache_index(b, g, slot, KV, capacity, d);
+                double *vx = cache_v + cache_index(b, g, slot, KV, capacity, d);
                 for (int i = 0; i < d; i++) {
                     kx[i] = k[((size_t)t * KV + g) * d + i];
                     vx[i] = v[((size_t)t * KV + g) * d + i];
@@ -232,11 +252,12 @@ int oracle_rope_append(int H, int KV, int d, int rd, int flags, double eps,
  *   ahead of the softmax);  p_j = exp(s_j - max s) / sum;  o = sum_j p_j v_j.
  * Keys before `first` are outside a sliding window (QwenAttnCfg.window, fn
  * attend_all_heads: first = stored - window) and get probability 0.
+ * Key j is read from slot j, or j mod capacity with a ring cache.
  * `scores` is scratch of length n; when `probs` is non-NULL it receives p_j
  * for j < n.  n == 0 leaves o at zero and writes no probabilities. */
 static void attend_one(const double *q, const double *keys, const double *vals, int n, int first,
-                       int d, double scale, double softcap, double *scores, double *o,
-                       double *probs)
+                       int d, double scale, double softcap, int flags, int capacity,
+                       double *scores, double *o, double *probs)
 {
     for (int i = 0; i < d; i++)
         o[i] = 0.0;
@@ -246,9 +267,10 @@ static void attend_one(const double *q, const double *keys, const double *vals, 
         first = 0;
     double m = -INFINITY;
     for (int j = first; j < n; j++) {
+        size_t kj = (size_t)slot_of(flags, j, capacity) * (size_t)d;
         double s = 0.0;
         for (int i = 0; i < d; i++)
-            s += q[i] * keys[(size_t)j * d + i];
+            s += q[i] * keys[kj + i];
         s *= scale;
         if (softcap > 0.0)
             s = softcap * tanh(s / softcap);
@@ -268,9 +290,24 @@ static void attend_one(const double *q, const double *keys, const double *vals, 
         double p = scores[j] / sum;
         if (probs)
             probs[j] = p;
+        size_t vj = (size_t)slot_of(flags, j, capacity) * (size_t)d;
         for (int i = 0; i < d; i++)
-            o[i] += p * vals[(size_t)j * d + i];
+            o[i] += p * vals[vj + i];
     }
+}
+
+/* Grow the score scratch to at least n entries (a ring's positions may run
+ * past its capacity).  Returns 0, or -1 when out of memory. */
+static int grow_scores(double **scores, size_t *size, int n)
+{
+    if ((size_t)n <= *size)
+        return 0;
+    double *p = (double *)realloc(*scores, sizeof(double) * (size_t)n);
+    if (!p)
+        return -1;
+    *scores = p;
+    *size = (size_t)n;
+    return 0;
 }
 
 /* cortiq fn apply_gate: o <- o * sigmoid(g). */
@@ -287,7 +324,12 @@ static void apply_gate(double *o, const double *g, int d)
  * inclusive of its own KV head kvh = h / (H / KV) -- only the last `window`
  * of them when window > 0 -- with scores soft-capped when softcap > 0.
  * Computed for the listed token indices only: out[r][h][d] for rows[r].
- * Returns 0, or -1 on a bad row or a position past the capacity. */
+ * With a ring cache (ORACLE_RING_CACHE, window > 0) the whole chunk is in the
+ * ring before any row attends, so a row's window must not reach a slot that a
+ * later token of its chunk overwrote: capacity >= window + (last new position
+ * of the sequence - pos).
+ * Returns 0, or -1 on a bad row, a position past a linear cache's capacity or
+ * a ring too small for the row's window. */
 int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
                        const int *cu_seqlens, const int *cache_lens, const double *q_rot,
                        const double *cache_k, const double *cache_v, int capacity,
@@ -295,9 +337,8 @@ int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
                        double softcap, int window)
 {
     int group = H / KV;
-    double *scores = (double *)malloc(sizeof(double) * (size_t)(capacity > 0 ? capacity : 1));
-    if (!scores)
-        return -1;
+    double *scores = NULL;
+    size_t scores_size = 0;
     for (int r = 0; r < nrows; r++) {
         int t = rows[r];
         int b = owner_of(batch, cu_seqlens, t);
@@ -306,7 +347,14 @@ int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
             return -1;
         }
         int pos = cache_lens[b] + (t - cu_seqlens[b]);
-        if (pos < 0 || pos >= capacity) {
+        int bad = pos < 0;
+        if (flags & ORACLE_RING_CACHE) {
+            int last = cache_lens[b] + (cu_seqlens[b + 1] - cu_seqlens[b]) - 1;
+            bad |= window <= 0 || (int64_t)capacity < (int64_t)window + (last - pos);
+        } else {
+            bad |= pos >= capacity;
+        }
+        if (bad || grow_scores(&scores, &scores_size, pos + 1) != 0) {
             free(scores);
             return -1;
         }
@@ -316,7 +364,8 @@ int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
             double *o = out + ((size_t)r * H + h) * d;
             attend_one(qv, cache_k + cache_index(b, kvh, 0, KV, capacity, d),
                        cache_v + cache_index(b, kvh, 0, KV, capacity, d), pos + 1,
-                       window > 0 ? pos + 1 - window : 0, d, scale, softcap, scores, o, NULL);
+                       window > 0 ? pos + 1 - window : 0, d, scale, softcap, flags, capacity,
+                       scores, o, NULL);
             if ((flags & ORACLE_OUT_GATE) && gate)
                 apply_gate(o, gate + ((size_t)t * H + h) * d, d);
         }
@@ -332,22 +381,26 @@ int oracle_attend_rows(int H, int KV, int d, double scale, int flags, int batch,
  * pairs listed in rows_bh (b * H + h) are computed when rows_bh is non-NULL;
  * otherwise all of them.  With window > 0 only the last `window` keys are
  * attended (the others get probability 0); softcap > 0 caps the scores.
- * Returns 0, or -1 when a length exceeds the capacity or the stride. */
+ * With a ring cache (ORACLE_RING_CACHE) key j sits in slot j mod capacity and
+ * the window must fit the ring (0 < window <= capacity).
+ * Returns 0, or -1 when a length exceeds a linear cache's capacity or the
+ * stride, or the window does not fit the ring. */
 int oracle_decode(int H, int KV, int d, double scale, int flags, int batch, const double *q,
                   const double *cache_k, const double *cache_v, int capacity,
                   const int *kv_lens, const double *gate, double *out, double *probs,
                   int probs_stride, int nrows, const int *rows_bh, double softcap, int window)
 {
     int group = H / KV;
-    double *scores = (double *)malloc(sizeof(double) * (size_t)(capacity > 0 ? capacity : 1));
-    if (!scores)
-        return -1;
+    double *scores = NULL;
+    size_t scores_size = 0;
     int count = rows_bh ? nrows : batch * H;
     for (int r = 0; r < count; r++) {
         int bh = rows_bh ? rows_bh[r] : r;
         int b = bh / H, h = bh % H;
         int n = kv_lens[b];
-        if (n < 0 || n > capacity || (probs && n > probs_stride)) {
+        int ring = (flags & ORACLE_RING_CACHE) != 0;
+        if (n < 0 || (!ring && n > capacity) || (ring && (window <= 0 || window > capacity)) ||
+            (probs && n > probs_stride) || grow_scores(&scores, &scores_size, n) != 0) {
             free(scores);
             return -1;
         }
@@ -355,7 +408,7 @@ int oracle_decode(int H, int KV, int d, double scale, int flags, int batch, cons
         double *o = out + ((size_t)b * H + h) * d;
         attend_one(q + ((size_t)b * H + h) * d, cache_k + cache_index(b, kvh, 0, KV, capacity, d),
                    cache_v + cache_index(b, kvh, 0, KV, capacity, d), n,
-                   window > 0 ? n - window : 0, d, scale, softcap, scores, o,
+                   window > 0 ? n - window : 0, d, scale, softcap, flags, capacity, scores, o,
                    probs ? probs + ((size_t)b * H + h) * (size_t)probs_stride : NULL);
         if ((flags & ORACLE_OUT_GATE) && gate && n > 0)
             apply_gate(o, gate + ((size_t)b * H + h) * d, d);

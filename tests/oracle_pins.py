@@ -137,6 +137,133 @@ def pin_yarn_reductions(o):
     assert np.all(np.diff(r) <= 1e-15), "ratio must fall monotonically"
 
 
+def pin_yarn_attention_factor(o):
+    """The multiplier on cos and sin (cortiq QwenAttnCfg.rope_scale, fn
+    rope_rotate_scaled): the YaRN paper's 0.1 ln(s) + 1 at the hand-computed
+    values of tests/golden/yarn_attn_factor.json; 1 without YaRN or with a
+    factor <= 1; a positive value given by the caller passes unchanged.  In the
+    append, the rotated dims of K come out scaled by exactly that factor (norm
+    times the factor) and the other dims unchanged."""
+    g = _golden("yarn_attn_factor.json")
+    for c in g["values"]:
+        _close(o.rope_attn_factor(True, c["factor"], 0.0), c["expected"], g["abs_tol"],
+               f"factor {c['factor']}")
+        _close(o.rope_attn_factor(True, c["factor"], -1.0), c["expected"], g["abs_tol"],
+               "negative selects the default")
+    br = g["branches"]
+    _close(o.rope_attn_factor(False, 4.0, 0.0), br["no_yarn_default"], 0.0, "no yarn")
+    for f in (1.0, 0.5):
+        _close(o.rope_attn_factor(True, f, 0.0), br["yarn_factor_at_most_one_default"], 0.0,
+               f"yarn factor {f}")
+    for v in br["given_value_passes_through"]:
+        _close(o.rope_attn_factor(True, 4.0, v), v, 0.0, "given value (yarn)")
+        _close(o.rope_attn_factor(False, 1.0, v), v, 0.0, "given value (plain)")
+    # through the append: one token, K of 16 dims with rotary 8 at position 300
+    rng = np.random.default_rng(31)
+    d, rd = 16, 8
+    inv = o.yarn_inv_freq(rd, 1e6, 4.0, 8192, 32.0, 1.0)
+    s = o.rope_attn_factor(True, 4.0, 0.0)
+    q = rng.standard_normal((1, 1, d))
+    k = rng.standard_normal((1, 1, d))
+    v = rng.standard_normal((1, 1, d))
+    ck = np.zeros((1, 1, 400, d))
+    cv = np.zeros((1, 1, 400, d))
+    q_rot = o.rope_append(1, 1, d, rd, 0, 0.0, inv, s, [0, 1], [300], q, k, v, None, None, ck, cv)
+    kr = ck[0, 0, 300]
+    _close(np.linalg.norm(kr[:rd]), 1.1386294361119890618 * np.linalg.norm(k[0, 0, :rd]), 1e-13,
+           "rotated K norm")
+    _close(kr[rd:], k[0, 0, rd:], 0.0, "K dims past rd")
+    _close(np.linalg.norm(q_rot[0, 0, :rd]),
+           1.1386294361119890618 * np.linalg.norm(q[0, 0, :rd]), 1e-13, "rotated Q norm")
+
+
+# ------------------------------------------------------------ ring cache ---
+
+def _simulated_ring(n_positions, capacity):
+    """Where a ring buffer puts positions 0, 1, ...: a write pointer that
+    starts at slot 0, advances by one slot per position and wraps to 0 at the
+    end (needle fn batch_attention's ring of kv_window positions)."""
+    slots, ptr = [], 0
+    for _ in range(n_positions):
+        slots.append(ptr)
+        ptr += 1
+        if ptr == capacity:
+            ptr = 0
+    return slots
+
+
+def pin_ring_slot_simulated(o):
+    """The oracle's ring slot of every position equals the slot a simulated
+    write pointer gives it, for rings of 1, 3, 128 and 448 slots."""
+    for cap in (1, 3, 128, 448):
+        sim = _simulated_ring(5 * cap + 7, cap)
+        got = [o.ring_slot(p, cap) for p in range(len(sim))]
+        assert got == sim, f"ring of {cap}: {got[:12]} vs {sim[:12]}"
+    assert o.ring_slot(32768 * 3 + 5, 32768) == 5
+
+
+def pin_ring_equals_linear_window(o):
+    """With a window W, a ring cache of window + chunk - 1 slots gives the same
+    chunked prefill rows and the same decode outputs and probabilities as a
+    linear cache (the ring holds every key a row can see); each appended
+    position lands in the simulated slot with the linear cache's value; a ring
+    one slot too small for the chunk is rejected."""
+    rng = np.random.default_rng(41)
+    H, KV, d, rd, W = 2, 1, 8, 8, 3
+    inv = o.rope_inv_freq(rd, 1e4)
+    prior, new = [9, 0], [4, 3]
+    R = W + max(new) - 1
+    cu = [0, new[0], new[0] + new[1]]
+    T = cu[-1]
+    q = rng.standard_normal((T, H, d))
+    k = rng.standard_normal((T, KV, d))
+    v = rng.standard_normal((T, KV, d))
+    L = 16
+    lin_k = rng.standard_normal((2, KV, L, d))
+    lin_v = rng.standard_normal((2, KV, L, d))
+    ring_k = np.full((2, KV, R, d), np.nan)
+    ring_v = np.full((2, KV, R, d), np.nan)
+    for b in range(2):
+        sim = _simulated_ring(prior[b], R)
+        for pos in range(prior[b]):
+            ring_k[b, :, sim[pos]] = lin_k[b, :, pos]
+            ring_v[b, :, sim[pos]] = lin_v[b, :, pos]
+    q_lin = o.rope_append(H, KV, d, rd, 0, 0.0, inv, 1.0, cu, prior, q, k, v, None, None,
+                          lin_k, lin_v)
+    q_ring = o.rope_append(H, KV, d, rd, o_ring(o), 0.0, inv, 1.0, cu, prior, q, k, v, None, None,
+                           ring_k, ring_v)
+    _close(q_ring, q_lin, 0.0, "rotated q")
+    for b in range(2):
+        sim = _simulated_ring(prior[b] + new[b], R)
+        for pos in range(prior[b], prior[b] + new[b]):
+            _close(ring_k[b, :, sim[pos]], lin_k[b, :, pos], 0.0, f"ring K slot of {pos}")
+            _close(ring_v[b, :, sim[pos]], lin_v[b, :, pos], 0.0, f"ring V slot of {pos}")
+    rows = list(range(T))
+    a = o.attend_rows(H, KV, d, 0.6, 0, cu, prior, q_lin, lin_k, lin_v, None, rows, window=W)
+    b_ = o.attend_rows(H, KV, d, 0.6, o_ring(o), cu, prior, q_lin, ring_k, ring_v, None, rows,
+                       window=W)
+    _close(b_, a, 0.0, "ring prefill rows")
+    lens = [p + n for p, n in zip(prior, new)]
+    qd = rng.standard_normal((2, H, d))
+    lo, lp = o.decode(H, KV, d, 0.6, 0, qd, lin_k, lin_v, lens, probs_stride=L, window=W)
+    ro, rp = o.decode(H, KV, d, 0.6, o_ring(o), qd, ring_k, ring_v, lens, probs_stride=L, window=W)
+    _close(ro, lo, 0.0, "ring decode out")
+    _close(rp, lp, 0.0, "ring decode probs")
+    small_k = np.zeros((2, KV, R - 1, d))
+    try:
+        o.attend_rows(H, KV, d, 0.6, o_ring(o), cu, prior, q_lin, small_k, small_k.copy(), None,
+                      rows, window=W)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a ring smaller than window + chunk - 1 must be rejected")
+
+
+def o_ring(o):
+    import oracle as oracle_mod
+    return oracle_mod.RING_CACHE
+
+
 # ----------------------------------------------------------------- norms ---
 
 def pin_rmsnorm_values(o):

@@ -28,8 +28,8 @@ MUTANTS = [
      "double inv = 1.0 / sqrt(ss / (double)d);\n    for (int i = 0; i < d; i++)\n        x[i] *= inv;", 1),
     ("zero_centred_swapped", "(zero_centered ? 1.0 + w[i] : w[i])", "(zero_centered ? w[i] : 1.0 + w[i])", 1),
     ("gate_sign", "o[i] *= 1.0 / (1.0 + exp(-g[i]));", "o[i] *= 1.0 / (1.0 + exp(g[i]));", 1),
-    ("position_ignores_prior", "int pos = cache_lens[b] + (t - cu_seqlens[b]);\n            if (pos < 0 || pos >= capacity)\n                return -1;",
-     "int pos = (t - cu_seqlens[b]);\n            if (pos < 0 || pos >= capacity)\n                return -1;", 1),
+    ("position_ignores_prior", "int pos = cache_lens[b] + (t - cu_seqlens[b]);\n            if (pos < 0 ||",
+     "int pos = (t - cu_seqlens[b]);\n            if (pos < 0 ||", 1),
     ("rope_scale_ignored", "x[i + half] = (x0 * s + x1 * c) * scale;", "x[i + half] = (x0 * s + x1 * c);", 1),
     ("k_not_normed", "oracle_rmsnorm_head(kx, k_norm_w, d, eps, zc);", "(void)zc;", 1),
     ("v_norm_on_k", "oracle_vnorm_head(vx, d, eps);", "oracle_vnorm_head(kx, d, eps);", 1),
@@ -40,6 +40,14 @@ MUTANTS = [
     ("decode_window_off_by_one", "window > 0 ? n - window : 0", "window > 0 ? n - window + 1 : 0", 1),
     ("prefill_window_off_by_one", "window > 0 ? pos + 1 - window : 0", "window > 0 ? pos - window : 0", 1),
     ("importance_overwrites", "*dst = accumulate ? *dst + s : s;", "*dst = s;", 1),
+    ("yarn_attn_factor_log10", "return 0.1 * log(factor) + 1.0;", "return 0.1 * log10(factor) + 1.0;", 1),
+    ("yarn_attn_factor_one_dropped", "return 0.1 * log(factor) + 1.0;", "return 0.1 * log(factor);", 1),
+    ("yarn_attn_factor_always_default", "if (attn_factor > 0.0)\n        return attn_factor;",
+     "if (attn_factor > 0.0)\n        return 1.0;", 1),
+    ("ring_slot_off_by_one", "return (int)(pos % (int64_t)capacity);",
+     "return (int)((pos + 1) % (int64_t)capacity);", 1),
+    ("ring_capacity_check_ignores_chunk", "(int64_t)capacity < (int64_t)window + (last - pos)",
+     "(int64_t)capacity < (int64_t)window", 1),
 ]
 
 
