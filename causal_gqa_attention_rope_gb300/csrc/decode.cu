@@ -301,7 +301,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
             if ((int)it - 1 - s < 0)
                 break;
             const uint32_t last = it - 1 - s;
-            mbar_wait_bounded(&sm.full[last % DEC_STAGES], (last / DEC_STAGES) & 1);
+            if (!mbar_wait_bounded(&sm.full[last % DEC_STAGES], (last / DEC_STAGES) & 1))
+                na_report(p.status, NA_ERR_DEVICE_TIMEOUT);
         }
         return;
     }
@@ -506,8 +507,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
             }
         }
         named_barrier_sync(1, DEC_CWARPS * 32);
+        // Every consumer warp has finished this piece's tiles (or given up): the
+        // abort flag is final for the piece.  A piece of a CTA whose wait gave up
+        // is written as the marker (max -inf, sum -1), which the merge passes
+        // report instead of merging, so no call ever merges another call's rows.
+        const bool bad = *(volatile int *)&sm.abort_flag != 0;
         for (int idx = threadIdx.x; idx < HPC * D; idx += DEC_CWARPS * 32) {
             const int h = idx / D, e = idx - h * D;
+            if (bad) {
+                if (e == 0) {
+                    const size_t row = (size_t)pc.id * HPC + h;
+                    p.part_ml[row * 2] = -INFINITY;
+                    p.part_ml[row * 2 + 1] = -1.0f;
+                }
+                continue;
+            }
             float M = -INFINITY;
 #pragma unroll
             for (int ww = 0; ww < DEC_CWARPS; ww++)
@@ -522,8 +536,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
                     l += sm.merge_l[ww][h] * f;
                 }
             }
-            if (aborted)
-                continue;
             const size_t row = (size_t)pc.id * HPC + h;
             p.part_o[row * D + e] = o;
             if (e == 0) {
@@ -531,7 +543,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
                 p.part_ml[row * 2 + 1] = l;
             }
         }
-        if (threadIdx.x == 0 && !aborted) {
+        if (threadIdx.x == 0) {  // the span follows from the slicing alone: always written
             const int stream = pc.id - blockIdx.x;
             if (pc.first)
                 p.piece_span[2 * stream] = pc.id;
@@ -546,11 +558,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) decode_split_kernel(const Deco
 // log2-domain (max, sum) pairs at ml[2 hpc s], ml[2 hpc s + 1].  Every lane of
 // the calling warp gets the same values: lanes take pieces lane, lane + 32, ...
 // and reduce with butterflies (a fixed order: the same result on every run and
-// in both merge passes).
-__device__ __forceinline__ void merge_weights_from(float m0, float l0, const float *ml, int hpc,
+// in both merge passes).  Returns false, on every lane, when a piece carries
+// the marker of a split-pass CTA whose wait gave up (a negative sum).
+__device__ __forceinline__ bool merge_weights_from(float m0, float l0, const float *ml, int hpc,
                                                    int ns, int lane, float &M, float &inv_l)
 {
     const unsigned FULL = 0xffffffffu;
+    bool bad = lane < ns && l0 < 0.f;
     M = m0;
     for (int s = lane + 32; s < ns; s += 32)
         M = fmaxf(M, ml[2 * hpc * s]);
@@ -559,14 +573,16 @@ __device__ __forceinline__ void merge_weights_from(float m0, float l0, const flo
         M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
     float L = m0 == -INFINITY ? 0.f : l0 * exp2f(m0 - M);
     for (int s = lane + 32; s < ns; s += 32) {
-        const float m = ml[2 * hpc * s];
+        const float m = ml[2 * hpc * s], l = ml[2 * hpc * s + 1];
+        bad |= l < 0.f;
         if (m != -INFINITY)
-            L += ml[2 * hpc * s + 1] * exp2f(m - M);
+            L += l * exp2f(m - M);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1)
         L += __shfl_xor_sync(FULL, L, o);
     inv_l = L > 0.f ? 1.0f / L : 0.f;
+    return !__any_sync(FULL, bad);
 }
 
 // The lane's own piece (lane < ns), loaded: (max, sum), or (-inf, 0).
@@ -581,12 +597,12 @@ __device__ __forceinline__ void merge_lane_piece(const float *ml, int hpc, int n
     }
 }
 
-__device__ __forceinline__ void merge_weights(const float *ml, int hpc, int ns, int lane, float &M,
+__device__ __forceinline__ bool merge_weights(const float *ml, int hpc, int ns, int lane, float &M,
                                               float &inv_l)
 {
     float m0, l0;
     merge_lane_piece(ml, hpc, ns, lane, m0, l0);
-    merge_weights_from(m0, l0, ml, hpc, ns, lane, M, inv_l);
+    return merge_weights_from(m0, l0, ml, hpc, ns, lane, M, inv_l);
 }
 
 // Element e of a head's merged output: the pieces' partial rows weighted by
@@ -689,7 +705,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     // Row maximum and sum over the pieces: every warp reduces them.
     const int lane = threadIdx.x & 31;
     float M, inv_l;
-    merge_weights(ml, hpc, ns, lane, M, inv_l);
+    if (!merge_weights(ml, hpc, ns, lane, M, inv_l)) {  // a split-pass wait gave up
+        if (threadIdx.x == 0)
+            na_report(p.status, NA_ERR_DEVICE_TIMEOUT);
+        for (int e = threadIdx.x; e < D; e += NT)
+            out[e] = __float2bfloat16_rn(0.f);
+        return;
+    }
 
     const float *po = p.part_o + row0 * D;
     for (int e = threadIdx.x; e < D; e += NT) {
@@ -821,12 +843,12 @@ __global__ void __launch_bounds__(kMiThreads) decode_merge_imp_kernel(const Deco
             const int h = hb + q * (kMiThreads / 32);
             if (h >= p.H)
                 break;  // warp-uniform
-            const bool ok = ns[q] >= 0;
+            bool ok = ns[q] >= 0;
             float M = -INFINITY, inv_l = 0.f;
             if (ok)
-                merge_weights_from(m0[q], l0[q], p.part_ml + (size_t)row0[q] * 2, hpc, ns[q], lane,
-                                   M, inv_l);
-            else if (lead && lane == 0)
+                ok = merge_weights_from(m0[q], l0[q], p.part_ml + (size_t)row0[q] * 2, hpc, ns[q],
+                                        lane, M, inv_l);
+            if (!ok && lead && lane == 0)
                 na_report(p.status, NA_ERR_DEVICE_TIMEOUT);
             if (lane == 0) {
                 sM[h] = M;

@@ -9,10 +9,16 @@
 //
 // The array is NA_STATIC_DECODE_SCRATCH_BYTES (20 MiB) and lives for as long as
 // the library is loaded, on every GPU that loads it.  All calls share it and it
-// keeps whatever the last call left there: the decode needs nothing in it to
-// start at zero (every partial it reads was written earlier in the same call),
-// but two calls whose kernels overlap on the GPU (different streams, or
-// several host threads) race on it and give wrong results.
+// keeps whatever the last call left there.  The decode needs nothing in it to
+// start at zero: the split pass writes every partial row and every stream's
+// piece span that the merge pass reads, in the same call -- a CTA whose wait
+// gave up writes a marker row that the merge pass reports instead of merging.
+// Two calls whose kernels overlap on the GPU (different streams, or several
+// host threads) race on it and give wrong results.
+//
+// The array's device address is looked up once per device and kept; a
+// cudaDeviceReset() of that device unloads the module and invalidates it, so
+// this entry point must not be called on a device after it was reset.
 #include <mutex>
 
 #include "na_internal.cuh"

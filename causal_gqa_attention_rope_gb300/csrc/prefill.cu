@@ -78,6 +78,15 @@ __device__ __forceinline__ void set_abort(int *flag, int32_t *status)
     na_report(status, NA_ERR_DEVICE_TIMEOUT);
 }
 
+// A bounded wait whose outcome is only reported: the drains before exit (copies
+// in flight, MMAs before tensor memory is released), where there is nothing
+// left to skip.  A wait that gives up writes NA_ERR_DEVICE_TIMEOUT.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, int32_t *status)
+{
+    if (!mbar_wait_bounded(bar, parity))
+        na_report(status, NA_ERR_DEVICE_TIMEOUT);
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c)
 {
     float r;
@@ -233,9 +242,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (eager) {  // let the early copies land, give the tensor memory back
             if (threadIdx.x == 0) {
                 if (early_q)
-                    mbar_wait_bounded(&sm.q_full, 0);
-                mbar_wait_bounded(&sm.k_full[0], 0);
-                mbar_wait_bounded(&sm.v_full[0], 0);
+                    drain_wait(&sm.q_full, 0, p.status);
+                drain_wait(&sm.k_full[0], 0, p.status);
+                drain_wait(&sm.v_full[0], 0, p.status);
             }
             tc::fence_before_sync();
             __syncthreads();
@@ -291,7 +300,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc::tma_load_2d(sm.k[st][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[st]);
                 if (!mbar_wait_bounded(&sm.v_empty[st], par) || aborted(&sm.abort_flag)) {
                     set_abort(&sm.abort_flag, p.status);
-                    mbar_wait_bounded(&sm.k_full[st], (j / STAGES) & 1);
+                    drain_wait(&sm.k_full[st], (j / STAGES) & 1, p.status);
                     break;
                 }
                 mbar_arrive_expect_tx(&sm.v_full[st], KB * BN * 128);
@@ -300,10 +309,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 issued = j + 1;
             }
             // every copy issued lands before the CTA can exit
-            mbar_wait_bounded(&sm.q_full, 0);
+            drain_wait(&sm.q_full, 0, p.status);
             for (int j = issued - 1; j >= 0 && j >= issued - STAGES; j--) {
-                mbar_wait_bounded(&sm.k_full[j % STAGES], (j / STAGES) & 1);
-                mbar_wait_bounded(&sm.v_full[j % STAGES], (j / STAGES) & 1);
+                drain_wait(&sm.k_full[j % STAGES], (j / STAGES) & 1, p.status);
+                drain_wait(&sm.v_full[j % STAGES], (j / STAGES) & 1, p.status);
             }
         }
     } else if (warp == 1) {
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 set_abort(&sm.abort_flag, p.status);
             if (any) {  // all issued MMAs complete before tensor memory is released
                 tc::mma_commit(&sm.drain[0]);
-                mbar_wait_bounded(&sm.drain[0], 0);
+                drain_wait(&sm.drain[0], 0, p.status);
             }
         }
     } else if (warp == 2) {
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 set_abort(&sm.abort_flag, p.status);
             if (any) {
                 tc::mma_commit(&sm.drain[1]);
-                mbar_wait_bounded(&sm.drain[1], 0);
+                drain_wait(&sm.drain[1], 0, p.status);
             }
         }
     } else if (warp >= 4) {

@@ -193,7 +193,12 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
  *   workspace  at least na_decode_workspace_size() bytes: partial results of
  *              every slice piece plus 8 bytes per (sequence, kv head, head
  *              chunk); its size depends on the batch and the head layout, not on
- *              the lengths.  Not read before the call writes it.
+ *              the lengths.  Not read before the call writes it (any contents
+ *              will do, also after a call that timed out).
+ *   status     device int32 or NULL: NA_ERR_CAPACITY for a length past the
+ *              capacity or max_kv_len (zero output), NA_ERR_DEVICE_TIMEOUT when
+ *              a wait of the split pass gave up (the affected heads get a zero
+ *              output and no probabilities).
  */
 int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
                    const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
@@ -217,11 +222,16 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
  *     NA_ERR_WORKSPACE before anything is enqueued (for 32 query heads and
  *     head_dim 128: a batch of up to about 1200 sequences, of any length).
  *   - The first call on a device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ *     device current) and keeps it; make that first call before any stream
+ *     capture.  A cudaDeviceReset() of the device invalidates the kept address:
+ *     do not call this entry point on a device after resetting it.
  *   - All calls share the array and it keeps the last call's contents; the
- *     decode needs nothing in it to start at zero.  Calls whose kernels overlap
- *     on the GPU (other streams, other host threads) race on the array: order
- *     them on one stream.
+ *     decode needs nothing in it to start at zero (the split pass writes every
+ *     partial result and piece span the merge pass reads, in the same call,
+ *     and a piece whose wait gave up is written as a marker that the merge
+ *     pass reports as NA_ERR_DEVICE_TIMEOUT, with a zero output, instead of
+ *     merging).  Calls whose kernels overlap on the GPU (other streams, other
+ *     host threads) race on the array: order them on one stream.
  */
 int na_attn_decode_static_ws(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
                              const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
