@@ -31,12 +31,25 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - 7)
 
 
+def ulp_tolerance(ref: np.ndarray) -> np.ndarray:
+    """One bf16 ulp of the reference value's own binade.  The one exception:
+    where the reference lies within half a step below a power of two, its
+    correctly rounded bf16 value is that power of two (round to nearest, ties
+    to the even significand, which the power of two has), and the tolerance is
+    one ulp of that value -- one step of the binade above."""
+    ax = np.abs(ref)
+    u = bf16_ulp(ref)
+    boundary = np.exp2(np.floor(np.log2(np.maximum(ax, np.finfo(np.float32).tiny))) + 1)
+    rounds_up = (boundary - ax) <= 0.5 * u
+    return np.where(rounds_up, 2.0 * u, u)
+
+
 def assert_within_ulp(gpu_bf16: torch.Tensor, ref: np.ndarray, what: str, ulps: float = 1.0):
     g = gpu_bf16.to(torch.float64).numpy()
     assert g.shape == ref.shape, f"{what}: shape {g.shape} vs {ref.shape}"
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
     err = np.abs(g - ref)
-    tol = ulps * np.maximum(bf16_ulp(ref), bf16_ulp(g))
+    tol = ulps * ulp_tolerance(ref)
     bad = err > tol
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} values beyond {ulps} ulp; "
                            f"worst {float((err / tol).max()):.3f} ulp-units")
@@ -59,6 +72,36 @@ def assert_probs_close(gpu: np.ndarray, ref: np.ndarray, what: str):
     err = float(np.max(np.abs(gpu - ref))) if gpu.size else 0.0
     assert err <= PROBS_MAX_ABS, f"{what}: probs max-abs {err:.3e} > {PROBS_MAX_ABS}"
     return err
+
+
+# ----------------------------------------------------------- guard bands ---
+# Every output buffer of a GPU parity case sits between two bands of a NaN
+# bit pattern (bf16 0x7FC1, fp32 0x7FC0DEAD); after the call the bands must be
+# bit for bit as they were: no kernel writes before or past its buffer.
+GUARD_ELEMS = 512  # per side: 1 KiB of bf16, 2 KiB of fp32 (keeps 16-byte alignment)
+_GUARD_BITS = {torch.bfloat16: (torch.int16, W.SENTINEL_BITS),
+               torch.float32: (torch.int32, 0x7FC0DEAD)}
+
+
+class Guarded:
+    """A device tensor of `shape` with guard bands on both sides; `t` is the
+    interior view handed to the library."""
+
+    def __init__(self, shape, dtype, device="cuda", fill=None):
+        self.n = int(np.prod(shape)) if len(shape) else 1
+        ity, bits = _GUARD_BITS[dtype]
+        self.buf = torch.empty(self.n + 2 * GUARD_ELEMS, dtype=dtype, device=device)
+        self.buf.view(ity).fill_(bits)
+        self.ity, self.bits = ity, bits
+        self.t = self.buf[GUARD_ELEMS:GUARD_ELEMS + self.n].view(shape)
+        if fill is not None:
+            self.t.copy_(fill) if torch.is_tensor(fill) else self.t.fill_(fill)
+
+    def check(self, what: str):
+        g = self.buf.view(self.ity)
+        lo, hi = g[:GUARD_ELEMS], g[GUARD_ELEMS + self.n:]
+        assert bool((lo == self.bits).all()), f"{what}: written before the buffer"
+        assert bool((hi == self.bits).all()), f"{what}: written past the end of the buffer"
 
 
 def sentinel_mask(t: torch.Tensor) -> torch.Tensor:
@@ -87,11 +130,12 @@ def score_scale(spec: W.Spec) -> float:
     return spec.sm_scale if spec.sm_scale > 0 else 1.0 / math.sqrt(spec.d)
 
 
-def oracle_flags(spec: W.Spec) -> int:
+def oracle_flags(spec: W.Spec, ring: bool = False) -> int:
     import oracle as O
     return ((O.QK_NORM if spec.qk_norm else 0)
             | (O.QK_NORM_ZERO_CENTERED if spec.qk_norm_zero_centered else 0)
-            | (O.V_NORM if spec.v_norm else 0) | (O.OUT_GATE if spec.out_gate else 0))
+            | (O.V_NORM if spec.v_norm else 0) | (O.OUT_GATE if spec.out_gate else 0)
+            | (O.RING_CACHE if ring else 0))
 
 
 # ------------------------------------------------------------- GPU runs ---
@@ -116,8 +160,8 @@ def gpu_step(step: W.StepInputs, device="cuda", max_total_len: Optional[int] = N
     qw, kw = dev(step.q_norm_w), dev(step.k_norm_w)
     cache = na.KVCache(dev(step.cache_k), dev(step.cache_v))
     T = step.total_tokens
-    q_out = torch.empty_like(q)
-    out = torch.empty_like(q)
+    gq, go = Guarded(q.shape, q.dtype, device), Guarded(q.shape, q.dtype, device)
+    q_out, out = gq.t, go.t
     status = torch.zeros(1, dtype=torch.int32, device=device)
     new = (step.cu_seqlens[1:] - step.cu_seqlens[:-1])
     max_new = int(new.max()) if new.numel() else 0
@@ -130,6 +174,8 @@ def gpu_step(step: W.StepInputs, device="cuda", max_total_len: Optional[int] = N
     na.na_attn_prefill_chunk(cfg, cu, lens, max_new, max_total_len, q_out, cache, out, gate=gate,
                              workspace=ws, status=status, total_tokens=T)
     torch.cuda.synchronize()
+    gq.check("q_out")
+    go.check("out")
     return GpuStep(q_out.cpu(), out.cpu(), cache.k.cpu(), cache.v.cpu(), int(status.item()))
 
 
@@ -158,12 +204,14 @@ def gpu_chunked(prompt: W.ChunkedPrompt, device="cuda"):
         n = hi - lo
         cu, lens, q, k, v = (x.to(device) for x in (cu, lens, q, k, v))
         gate = None if gate is None else gate.to(device)
-        q_out = torch.empty_like(q)
-        out = torch.empty_like(q)
+        gq, go = Guarded(q.shape, q.dtype, device), Guarded(q.shape, q.dtype, device)
+        q_out, out = gq.t, go.t
         na.na_rope_append_kv(cfg, rope, cu, lens, q, k, v, q_out, cache, q_norm_w=qw, k_norm_w=kw,
                              status=status)
         na.na_attn_prefill_chunk(cfg, cu, lens, n, hi, q_out, cache, out, gate=gate, workspace=ws,
                                  status=status)
+        gq.check(f"q_out of chunk {c}")
+        go.check(f"out of chunk {c}")
         outs.append(out.view(B, n, s.H, s.d).cpu())
         qrots.append(q_out.view(B, n, s.H, s.d).cpu())
     torch.cuda.synchronize()
@@ -182,16 +230,21 @@ def gpu_decode(dec: W.DecodeInputs, device="cuda", with_probs=True, num_splits=0
     cache = na.KVCache(dec.cache_k.to(device), dec.cache_v.to(device))
     kv = dec.kv_lens.to(device)
     gate = None if dec.gate is None else dec.gate.to(device)
-    out = torch.empty_like(q)
+    go = Guarded(q.shape, q.dtype, device)
+    out = go.t
     stride = probs_stride or max(max_kv, 1)
-    probs = None
+    probs, gp = None, None
     if with_probs:
-        probs = torch.full((B, s.H, stride), -7.0, dtype=torch.float32, device=device)
+        gp = Guarded((B, s.H, stride), torch.float32, device, fill=-7.0)
+        probs = gp.t
     ws = na.workspace(na.na_decode_workspace_size(cfg, B, max_kv, num_splits), device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
     na.na_attn_decode(cfg, q, cache, kv, max_kv, out, probs=probs, gate=gate, workspace=ws,
                       num_splits=num_splits, status=status)
     torch.cuda.synchronize()
+    go.check("decode out")
+    if gp is not None:
+        gp.check("decode probs")
     return out.cpu(), (None if probs is None else probs.cpu()), int(status.item())
 
 
@@ -206,22 +259,25 @@ class OracleStep:
     inv_freq: np.ndarray
 
 
-def oracle_append(o, step: W.StepInputs) -> OracleStep:
+def oracle_append(o, step: W.StepInputs, ring: bool = False) -> OracleStep:
+    """The oracle's append of the step's new tokens into (a copy of) its cache;
+    with ring=True the step's cache is a ring (slot = position mod capacity)."""
     s = step.spec
     inv = o.inv_freq_for(s.rope.as_dict(), s.rd)
     scale = o.rope_attn_factor(s.rope.yarn, s.rope.factor, s.rope.attn_factor)
     ck = np.ascontiguousarray(W.bf16_to_f64(step.cache_k))
     cv = np.ascontiguousarray(W.bf16_to_f64(step.cache_v))
-    q_rot = o.rope_append(s.H, s.KV, s.d, s.rd, oracle_flags(s), s.eps, inv, scale,
+    q_rot = o.rope_append(s.H, s.KV, s.d, s.rd, oracle_flags(s, ring), s.eps, inv, scale,
                           step.cu_seqlens.numpy(), step.cache_lens.numpy(),
                           W.bf16_to_f64(step.q), W.bf16_to_f64(step.k), W.bf16_to_f64(step.v),
                           W.bf16_to_f64(step.q_norm_w), W.bf16_to_f64(step.k_norm_w), ck, cv)
     return OracleStep(q_rot, ck, cv, scale, inv)
 
 
-def oracle_rows(o, step: W.StepInputs, ost: OracleStep, rows: Sequence[int]) -> np.ndarray:
+def oracle_rows(o, step: W.StepInputs, ost: OracleStep, rows: Sequence[int],
+                ring: bool = False) -> np.ndarray:
     s = step.spec
-    return o.attend_rows(s.H, s.KV, s.d, score_scale(s), oracle_flags(s),
+    return o.attend_rows(s.H, s.KV, s.d, score_scale(s), oracle_flags(s, ring),
                          step.cu_seqlens.numpy(), step.cache_lens.numpy(), ost.q_rot,
                          ost.cache_k, ost.cache_v, W.bf16_to_f64(step.gate), list(rows),
                          softcap=s.softcap, window=s.window)
@@ -275,13 +331,14 @@ def sample_rows(n: int, k: int, seed: int) -> List[int]:
     return sorted(set([0, n - 1] + mid.tolist()))
 
 
-def ring_from_linear(cache: torch.Tensor, lens: Sequence[int], ring: int) -> torch.Tensor:
+def ring_from_linear(o, cache: torch.Tensor, lens: Sequence[int], ring: int) -> torch.Tensor:
     """A linear cache [B, KV, cap, d] laid out as a ring of `ring` slots per
-    (sequence, kv head): position p of the first lens[b] lives in slot p % ring
-    (only the last `ring` positions survive); untouched slots hold the sentinel."""
+    (sequence, kv head): position p of the first lens[b] goes to the oracle's
+    ring slot of p, so only the last `ring` positions survive; untouched slots
+    hold the sentinel."""
     B, KV, _, d = cache.shape
     out = W.sentinel_fill((B, KV, ring, d))
     for b, n in enumerate(lens):
         for pos in range(max(0, n - ring), n):
-            out[b, :, pos % ring] = cache[b, :, pos]
+            out[b, :, o.ring_slot(pos, ring)] = cache[b, :, pos]
     return out

@@ -4,15 +4,15 @@ import pytest
 import torch
 
 import workloads as W
-from harness import (assert_out_close, assert_probs_close, gpu_decode, oracle_flags, sample_rows,
-                     score_scale)
+from harness import (Guarded, assert_out_close, assert_probs_close, gpu_decode, oracle_flags,
+                     sample_rows, score_scale)
 
 pytestmark = pytest.mark.gpu
 
 
-def _oracle_decode(oracle, dec, rows_bh=None, stride=None):
+def _oracle_decode(oracle, dec, rows_bh=None, stride=None, ring=False):
     s = dec.spec
-    return oracle.decode(s.H, s.KV, s.d, score_scale(s), oracle_flags(s), W.bf16_to_f64(dec.q),
+    return oracle.decode(s.H, s.KV, s.d, score_scale(s), oracle_flags(s, ring), W.bf16_to_f64(dec.q),
                          np.ascontiguousarray(W.bf16_to_f64(dec.cache_k)),
                          np.ascontiguousarray(W.bf16_to_f64(dec.cache_v)), dec.kv_lens.numpy(),
                          gate=W.bf16_to_f64(dec.gate), probs_stride=stride, rows_bh=rows_bh,
@@ -90,19 +90,25 @@ def test_decode_ring_cache(oracle):
     dev = "cuda"
     cfg = attn_cfg(spec)
     cfg.ring_cache = True
-    cache = na.KVCache(ring_from_linear(dec.cache_k, lens, R).to(dev),
-                       ring_from_linear(dec.cache_v, lens, R).to(dev))
+    rk = ring_from_linear(oracle, dec.cache_k, lens, R)
+    rv = ring_from_linear(oracle, dec.cache_v, lens, R)
+    cache = na.KVCache(rk.to(dev), rv.to(dev))
     q = dec.q.to(dev)
-    out = torch.empty_like(q)
     B, mx = len(lens), max(lens)
-    probs = torch.full((B, spec.H, mx), -7.0, dtype=torch.float32, device=dev)
+    go = Guarded(q.shape, q.dtype, dev)
+    gp = Guarded((B, spec.H, mx), torch.float32, dev, fill=-7.0)
+    out, probs = go.t, gp.t
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = na.workspace(na.na_decode_workspace_size(cfg, B, mx), dev)
     na.na_attn_decode(cfg, q, cache, dec.kv_lens.to(dev), mx, out, probs=probs, workspace=ws,
                       status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    ref_out, ref_p = _oracle_decode(oracle, dec, stride=mx)
+    go.check("ring decode out")
+    gp.check("ring decode probs")
+    # the oracle reads the same ring (key j in its ring slot of j)
+    ring_dec = W.DecodeInputs(**{**dec.__dict__, "cache_k": rk, "cache_v": rv})
+    ref_out, ref_p = _oracle_decode(oracle, ring_dec, stride=mx, ring=True)
     assert_out_close(out.cpu().double().numpy(), ref_out, "ring decode out")
     for b, n in enumerate(lens):
         assert_probs_close(probs[b, :, :n].cpu().numpy(), ref_p[b, :, :n], f"ring probs {b}")
@@ -156,12 +162,14 @@ def _gpu_importance(dec, probs_cpu, imp_init, accumulate):
     import causal_gqa_attention_rope_gb300 as na
     from harness import attn_cfg
     dev = "cuda"
-    imp = imp_init.clone().to(dev)
+    gi = Guarded(tuple(imp_init.shape), torch.float32, dev, fill=imp_init.to(dev))
+    imp = gi.t
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     max_kv = int(dec.kv_lens.max())
     na.na_decode_importance(attn_cfg(dec.spec), probs_cpu.to(dev), dec.kv_lens.to(dev), max_kv,
                             imp, accumulate=accumulate, status=status)
     torch.cuda.synchronize()
+    gi.check("importance")
     return imp.cpu(), int(status.item())
 
 
@@ -283,14 +291,18 @@ def _gpu_decode_imp(dec, probs_stride=None, imp_init=None, accumulate=False, num
     cache = na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev))
     kv = dec.kv_lens.to(dev)
     gate = None if dec.gate is None else dec.gate.to(dev)
-    out = torch.empty_like(q)
-    probs = torch.full((B, s.H, stride), -7.0, dtype=torch.float32, device=dev)
-    imp = imp_init.clone().to(dev)
+    go = Guarded(q.shape, q.dtype, dev)
+    gp = Guarded((B, s.H, stride), torch.float32, dev, fill=-7.0)
+    gi = Guarded(tuple(imp_init.shape), torch.float32, dev, fill=imp_init.to(dev))
+    out, probs, imp = go.t, gp.t, gi.t
     ws = na.workspace(na.na_decode_workspace_size(cfg, B, max_kv, num_splits), dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     na.na_attn_decode_imp(cfg, q, cache, kv, max_kv, out, probs, imp, accumulate=accumulate,
                           gate=gate, workspace=ws, num_splits=num_splits, status=status)
     torch.cuda.synchronize()
+    go.check("decode_imp out")
+    gp.check("decode_imp probs")
+    gi.check("decode_imp importance")
     return out.cpu(), probs.cpu(), imp.cpu(), int(status.item())
 
 

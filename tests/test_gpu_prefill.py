@@ -5,8 +5,8 @@ import pytest
 import torch
 
 import workloads as W
-from harness import (assert_out_close, check_cache, gpu_chunked, gpu_step, oracle_append,
-                     oracle_rows, prompt_as_step, sample_rows)
+from harness import (Guarded, assert_out_close, check_cache, gpu_chunked, gpu_step,
+                     oracle_append, oracle_rows, prompt_as_step, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -139,7 +139,8 @@ def test_prefill_short_chunks(oracle, name):
 def test_prefill_ring_cache(oracle):
     """Ring cache (slot = position % capacity) with a window: the chunk is
     appended into the ring, every row attends the last `window` keys, and the
-    ring holds exactly the newest `capacity` positions afterwards."""
+    ring holds exactly the newest `capacity` positions afterwards.  The oracle
+    appends into and attends from the same ring."""
     import causal_gqa_attention_rope_gb300 as na
     from harness import (attn_cfg, oracle_append, oracle_rows, ring_from_linear, rope_cfg,
                          assert_within_ulp)
@@ -150,11 +151,14 @@ def test_prefill_ring_cache(oracle):
     dev = "cuda"
     cfg = attn_cfg(spec)
     cfg.ring_cache = True
-    ck, cv = ring_from_linear(step.cache_k, prior, R), ring_from_linear(step.cache_v, prior, R)
+    ck = ring_from_linear(oracle, step.cache_k, prior, R)
+    cv = ring_from_linear(oracle, step.cache_v, prior, R)
+    ring_step = W.StepInputs(**{**step.__dict__, "cache_k": ck, "cache_v": cv})
     cache = na.KVCache(ck.clone().to(dev), cv.clone().to(dev))
     q, k, v = step.q.to(dev), step.k.to(dev), step.v.to(dev)
     cu, lens = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
-    q_out, out = torch.empty_like(q), torch.empty_like(q)
+    gq, go = Guarded(q.shape, q.dtype, dev), Guarded(q.shape, q.dtype, dev)
+    q_out, out = gq.t, go.t
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     T = step.total_tokens
     max_new, max_tot = max(new), max(p + n for p, n in zip(prior, new))
@@ -164,22 +168,22 @@ def test_prefill_ring_cache(oracle):
                              status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    ost = oracle_append(oracle, step)
-    ref = oracle_rows(oracle, step, ost, list(range(T)))
+    gq.check("ring q_out")
+    go.check("ring out")
+    ost = oracle_append(oracle, ring_step, ring=True)
+    ref = oracle_rows(oracle, ring_step, ost, list(range(T)), ring=True)
     assert_out_close(out.cpu().double().numpy(), ref, "ring prefill")
     gk, gv = cache.k.cpu(), cache.v.cpu()
     for b in range(3):
         end = prior[b] + new[b]
-        for pos in range(max(0, end - R), end):
-            slot = pos % R
-            if pos >= prior[b]:  # appended now
-                assert_within_ulp(gk[b, :, slot], ost.cache_k[b, :, pos], f"ring K {b},{pos}")
-                assert np.array_equal(gv[b, :, slot].double().numpy(), ost.cache_v[b, :, pos])
-            else:  # history kept
-                assert torch.equal(gk[b, :, slot].view(torch.int16),
-                                   step.cache_k[b, :, pos].view(torch.int16))
-        for slot in range(end, R):  # never written
-            assert torch.equal(gk[b, :, slot].view(torch.int16), ck[b, :, slot].view(torch.int16))
+        written = {oracle.ring_slot(pos, R) for pos in range(prior[b], end)}
+        for slot in range(R):
+            if slot in written:  # appended now: the oracle's ring slot, within 1 ulp
+                assert_within_ulp(gk[b, :, slot], ost.cache_k[b, :, slot], f"ring K {b},{slot}")
+                assert np.array_equal(gv[b, :, slot].double().numpy(), ost.cache_v[b, :, slot])
+            else:  # history (or the sentinel) kept bit for bit
+                assert torch.equal(gk[b, :, slot].view(torch.int16), ck[b, :, slot].view(torch.int16))
+                assert torch.equal(gv[b, :, slot].view(torch.int16), cv[b, :, slot].view(torch.int16))
 
 
 def test_prefill_varlen_small_all_rows(oracle):
