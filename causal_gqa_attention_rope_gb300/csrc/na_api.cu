@@ -122,16 +122,19 @@ int check_rope(const na_rope_params *r)
 }
 
 struct PrefillPlan {
-    int pack, tile_tokens, q_tiles, num_splits, split_len;
+    int pack, tile_tokens, q_tiles, full_units, tail_units, num_splits, split_len, grid;
     size_t ws_bytes;
 };
 
-// Split the keys across CTAs only when the (query tile, head, sequence)
-// grid would leave most SMs idle (one CTA owns an SM).  The split count keeps
-// the grid within one wave (est * splits <= SMs: a 5-way split of 32 tiles on
-// 152 SMs left 8 CTAs for a second wave and measured ~2x slower than 4-way),
-// each split covering at least four key tiles (fewer, longer splits measured
-// faster than more, shorter ones: less partial traffic for the combine pass).
+// Units (query tile, head group, sequence) run one per CTA, at one CTA per
+// SM, in the order of the grid (heaviest query tiles first within a head, the
+// longest sequences first): the hardware starts each on the next free SM, and
+// the units streaming the same K/V run side by side.  Only the units left over
+// after the last whole wave -- or all of them when there are fewer than SMs --
+// are cut into up to SMs / units equal key ranges, at least four key tiles
+// each, so that the last wave keeps every SM busy (640 units of a long
+// context chunk on 152 SMs left 120 SMs idle for most of a fifth wave); a
+// merge pass combines the pieces of those units.
 PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int max_new_len,
                          int max_total_len)
 {
@@ -149,8 +152,10 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
         pl.pack = 1;
     pl.tile_tokens = bm / pl.pack;
     pl.q_tiles = (max_new_len + pl.tile_tokens - 1) / pl.tile_tokens;
-    const long long est = (long long)batch * pl.q_tiles * (c->num_heads / pl.pack);
-    const long long target = sm_count();
+    const long long units = (long long)batch * pl.q_tiles * (c->num_heads / pl.pack);
+    const long long sms = sm_count();
+    pl.full_units = (int)(units >= sms ? units - units % sms : 0);
+    pl.tail_units = (int)(units - pl.full_units);
     // Keys one tile can see: all history, or with a sliding window at most the
     // window plus the tile's own tokens (from the key tile holding the first
     // row's window start).
@@ -160,8 +165,8 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
         span = w < span ? w : span;
     }
     int splits = 1;
-    if (est < target && span > 4 * bn) {
-        splits = (int)(target / est);
+    if (pl.tail_units > 0 && span > 4 * bn) {
+        splits = (int)(sms / pl.tail_units);
         const int max_by_len = (int)((span + 4 * bn - 1) / (4 * bn));
         splits = splits < max_by_len ? splits : max_by_len;
         if (splits < 1)
@@ -176,9 +181,10 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
         pl.split_len = span > 0 ? (int)span : 1;
         pl.num_splits = 1;
     }
-    pl.ws_bytes = pl.num_splits > 1
-                      ? (size_t)total_tokens * c->num_heads * pl.num_splits * (c->head_dim + 2) * 4
-                      : 0;
+    pl.grid = pl.full_units + pl.tail_units * pl.num_splits;
+    pl.ws_bytes = pl.num_splits > 1 ? (size_t)pl.tail_units * pl.num_splits * bm *
+                                          (c->head_dim + 2) * sizeof(float)
+                                    : 0;
     return pl;
 }
 
@@ -352,6 +358,9 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
     p.pack = pl.pack;
     p.tile_tokens = pl.tile_tokens;
     p.q_tiles = pl.q_tiles;
+    p.HG = p.H / pl.pack;
+    p.full_units = pl.full_units;
+    p.tail_units = pl.tail_units;
     p.split_len = pl.split_len;
     p.num_splits = pl.num_splits;
     p.flags = cfg->flags;
@@ -364,7 +373,7 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
     p.out = static_cast<bf16 *>(out);
     if (pl.ws_bytes > 0) {
         p.part_o = static_cast<float *>(workspace);
-        p.part_ml = p.part_o + (size_t)total_tokens * p.H * pl.num_splits * cfg->head_dim;
+        p.part_ml = p.part_o + (size_t)pl.tail_units * pl.num_splits * prefill_q_tile() * cfg->head_dim;
     }
     p.status = status;
     return launch_prefill(p, cfg->head_dim, total_tokens, cache->batch,

@@ -269,14 +269,17 @@ struct PrefillParams {
     int pack;                  // query heads of one kv group per tile (a power of two)
     int tile_tokens;           // tokens per tile: 128 / pack
     int q_tiles;               // ceil(max_new_len / tile_tokens)
-    int split_len;             // keys per KV split (multiple of the key tile), or 0 = no split
-    int num_splits;
+    int HG;                    // head groups per sequence: H / pack
+    int full_units;            // units (query tile, head group, sequence) run whole, one CTA each
+    int tail_units;            // the units after them, each cut into num_splits key ranges
+    int split_len;             // keys per piece of a cut unit (multiple of the key tile)
+    int num_splits;            // pieces per cut unit (1: the tail units run whole too)
     uint32_t flags;
     const int32_t *cu_seqlens, *cache_lens;
     const bf16 *q, *cache_k, *cache_v, *gate;
     bf16 *out;
-    float *part_o;             // [T][H][num_splits][d]
-    float *part_ml;            // [T][H][num_splits][2]
+    float *part_o;             // [tail_units][num_splits][128][d]: rows of the pieces
+    float *part_ml;            // [tail_units][num_splits][128][2]: (max, sum), log2 domain
     int32_t *status;
 };
 

@@ -138,11 +138,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         sm.abort_flag = 0;
         fence_barrier_init();
     }
+    // The block's unit: CTAs 0 .. full_units - 1 take whole units, the rest one
+    // of num_splits key ranges of a tail unit.  Units run in the order
+    // (query tile, head group, sequence slot), heaviest query tiles first.
+    const int idx = blockIdx.x;
+    const bool in_tail = idx >= p.full_units;
+    const int nsplit = in_tail ? p.num_splits : 1;
+    const int tail_unit = in_tail ? (idx - p.full_units) / p.num_splits : 0;
+    const int split = in_tail ? (idx - p.full_units) - tail_unit * p.num_splits : 0;
+    const int unit = in_tail ? p.full_units + tail_unit : idx;
+    const int hg = (unit / p.q_tiles) % p.HG;
+    const int slot = unit / (p.q_tiles * p.HG);
+    const int qt = p.q_tiles - 1 - (unit % p.q_tiles);  // heaviest (latest) query tiles first
     // A tile that certainly has rows -- a sequence's first, or with a single
     // sequence any tile below the host-known token count -- takes the tensor
     // memory before the wait and issues its first copies speculatively.
     // Other tiles may be empty padding; they check first and leave at once.
-    const int qt = p.q_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
     const bool eager = p.batch == 1 && p.window == 0 && qt * p.tile_tokens < p.total_tokens;
     if (eager && warp == 1)
         tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
@@ -153,11 +164,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // The 128 rows are tile_tokens tokens x pack query heads of one kv group,
     // token-major: row r is token r >> pack_shift, head h0 + (r & (pack - 1)).
     const int pack_shift = __ffs(p.pack) - 1;
-    const int h0 = blockIdx.y * p.pack;
-    const int slot = blockIdx.z / p.num_splits, split = blockIdx.z - slot * p.num_splits;
+    const int h0 = hg * p.pack;
     const int kvh = h0 / p.group;
     const int r0 = qt * p.tile_tokens;  // first token of the tile within the sequence
-    const int split_off = p.num_splits > 1 ? split * p.split_len : 0;
+    const int split_off = nsplit > 1 ? split * p.split_len : 0;
     // The sequence this block serves.  With several sequences (up to 32) the
     // slots go to sequences in order of decreasing end position (prior + new
     // tokens), so the longest tiles start first (list scheduling of this
@@ -222,11 +232,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         return kv_row0 + (ring ? k % p.capacity : k);
     };
     int k_end = pos_hi + 1;
-    if (p.num_splits > 1)
+    if (nsplit > 1)
         k_end = min(k_end, k_begin + p.split_len);
     bool run = true;  // uniform over the CTA
     if (n_new > p.max_new_len || (b == 0 && tok0 != 0)) {
-        if (qt == 0 && blockIdx.y == 0 && split == 0 && threadIdx.x == 0)
+        if (qt == 0 && hg == 0 && split == 0 && threadIdx.x == 0)
             na_report(p.status, NA_ERR_INVALID_ARG);
         run = false;
     } else if (r0 >= n_new) {
@@ -526,7 +536,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // requested now so their latency overlaps the last P V product
         // (loaded one row at a time they cost ~25 us per CTA).
         constexpr int GW = D / 64;  // 32-bit words of gate per lane and row
-        const bool gated = ok && p.num_splits == 1 && (p.flags & NA_OUT_GATE) && p.gate;
+        const bool gated = ok && nsplit == 1 && (p.flags & NA_OUT_GATE) && p.gate;
         uint32_t gpre[32][GW];
         if (gated) {
 #pragma unroll
@@ -561,7 +571,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr int LDS = D + 4;
             constexpr int EPL = D / 32;  // elements per lane in the row stores
             float *stage = reinterpret_cast<float *>(&sm.k[0][0][0]);
-            const bool split_out = p.num_splits > 1;
+            const bool split_out = nsplit > 1;
+            // rows of this piece in the workspace: [tail unit][split][row]
+            const size_t piece_row0 = ((size_t)tail_unit * p.num_splits + split) * BM;
             const float scale = split_out ? 1.0f : (l > 0.f ? 1.0f / l : 0.f);
             {
                 uint32_t o[D / 32][32];  // the whole row in one round of loads
@@ -581,10 +593,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (split_out && r < rows) {
-                const size_t row = ((size_t)(tok0 + r0 + (r >> pack_shift)) * p.H + h0 +
-                                    (r & (p.pack - 1))) * p.num_splits + split;
-                p.part_ml[row * 2] = m_ref;
-                p.part_ml[row * 2 + 1] = l;
+                p.part_ml[(piece_row0 + r) * 2] = m_ref;
+                p.part_ml[(piece_row0 + r) * 2 + 1] = l;
             }
             __syncwarp();
             // One row per step, lanes across the row.
@@ -606,7 +616,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     v[1] = x.y;
                 }
                 if (split_out) {
-                    float *dst = p.part_o + ((tok * p.H + h) * p.num_splits + split) * D + lane * EPL;
+                    float *dst = p.part_o + (piece_row0 + rr) * D + lane * EPL;
                     if constexpr (EPL == 4)
                         *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
                     else
@@ -656,124 +666,145 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// Merge the KV splits of each (token, head) row: one warp per row.  The
-// owner sequence and every split's (max, sum) are read in one round (lane s
-// holds split s), then each lane reads its D/32 output elements of every split
-// with all the loads in flight at once.
+// The sequence that grid slot `slot` serves, and its bounds: with 2 to 32
+// sequences the slots go to sequences in order of decreasing end position
+// (prior + new tokens), as in the attention pass; otherwise slot b is
+// sequence b.  Called by a full warp; every lane gets the same values.
+__device__ __forceinline__ void slot_sequence(const PrefillParams &p, int slot, int lane, int &b,
+                                              int &tok0, int &n_new, int &prior)
+{
+    if (p.batch > 1 && p.batch <= 32) {
+        int c0 = 0, c1 = 0, pl = 0, key = -1;
+        if (lane < p.batch) {
+            c0 = __ldg(p.cu_seqlens + lane);
+            c1 = __ldg(p.cu_seqlens + lane + 1);
+            pl = __ldg(p.cache_lens + lane);
+            key = pl + (c1 - c0);
+        }
+        int rank = 0;
+        for (int j = 0; j < p.batch; j++) {
+            const int kj = __shfl_sync(0xffffffffu, key, j);
+            rank += (kj > key) || (kj == key && j < lane);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, lane < p.batch && rank == slot);
+        const int src = __ffs(m) - 1;
+        b = src;
+        tok0 = __shfl_sync(0xffffffffu, c0, src);
+        n_new = __shfl_sync(0xffffffffu, c1, src) - tok0;
+        prior = __shfl_sync(0xffffffffu, pl, src);
+        return;
+    }
+    b = slot;
+    tok0 = __ldg(p.cu_seqlens + b);
+    n_new = __ldg(p.cu_seqlens + b + 1) - tok0;
+    prior = __ldg(p.cache_lens + b);
+}
+
+// Merge pass of the cut (tail) units: CTA (u, g) merges rows 8 g .. 8 g + 7
+// of tail unit u, one warp per row.  Lane s loads piece s's (max, sum) (one
+// round), the row's M and L come from warp reductions, then each lane loads
+// its D/32 output elements of every piece's row, four pieces in flight at a
+// time, weights them by 2^(m_s - M) in piece order, normalises and gates.
+constexpr int kMergeRows = 8;
+
 template <int D>
-__global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParams p, int total_tokens)
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParams p)
 {
     constexpr int EPL = D / 32;  // output elements per lane
     grid_dependency_wait();
     grid_dependents_launch();
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
-    if (row >= total_tokens * p.H)
+    const int tu = blockIdx.x;
+    const int unit = p.full_units + tu;
+    const int hg = (unit / p.q_tiles) % p.HG;
+    const int slot = unit / (p.q_tiles * p.HG);
+    const int qt = p.q_tiles - 1 - (unit % p.q_tiles);
+    int b, tok0, n_new, prior;
+    slot_sequence(p, slot, lane, b, tok0, n_new, prior);
+    const int r0 = qt * p.tile_tokens;
+    const bool ring = (p.flags & NA_RING_CACHE) != 0;
+    if (n_new > p.max_new_len || (b == 0 && tok0 != 0) || r0 >= n_new)
+        return;  // invalid bounds were reported by the attention pass
+    const int rows_tok = min(p.tile_tokens, n_new - r0);
+    const int pos_lo = prior + r0, pos_hi = pos_lo + rows_tok - 1;
+    if (prior < 0 || (!ring && pos_hi >= p.capacity) || pos_hi >= p.max_total_len)
         return;
-    const int t = row / p.H;
-    const float *ml = p.part_ml + (size_t)row * p.num_splits * 2;
-    const float2 ml0 = lane < p.num_splits ? *reinterpret_cast<const float2 *>(ml + 2 * lane)
-                                           : make_float2(-INFINITY, 0.f);
-    // Owner sequence: the last b with cu_seqlens[b] <= t, a warp at a time.
-    int b = 0, pos = -1, rt = 0;  // rt: the token's index within its sequence
-    for (int base = 0; base < p.batch; base += 32) {
-        const int i = base + lane;
-        int cu = 0x7fffffff, cl = 0;
-        if (i < p.batch) {
-            cu = __ldg(p.cu_seqlens + i);
-            cl = __ldg(p.cache_lens + i);
-        }
-        const unsigned m = __ballot_sync(FULL, cu <= t);
-        if (m) {
-            const int src = 31 - __clz(m);
-            b = base + src;
-            rt = t - __shfl_sync(FULL, cu, src);
-            pos = __shfl_sync(FULL, cl, src) + rt;
-        }
-        if (m != FULL)
-            break;
-    }
-    if (pos < 0 || (!(p.flags & NA_RING_CACHE) && pos >= p.capacity) || pos >= p.max_total_len)
-        return;  // reported by the split pass
-    // Splits start at the key tile holding the window start of the row's query
-    // tile (0 without a window), as in the split pass.
-    int win_tile = 0;
-    if (p.window > 0) {
-        const int tile_pos_lo = pos - rt % p.tile_tokens;
-        win_tile = max(0, tile_pos_lo - p.window + 1) / BN * BN;
-    }
-    const int ns = min(p.num_splits, (pos - win_tile) / p.split_len + 1);
-
-    // Global maximum and sum over the splits this row has keys in.
+    const int pack_shift = __ffs(p.pack) - 1;
+    const int r = blockIdx.y * kMergeRows + warp;
+    if (r >= (rows_tok << pack_shift))
+        return;
+    // pieces with keys: the splits start at the key tile holding the first
+    // row's window start (0 without a window), split_len keys apart
+    const int win_tile = p.window > 0 ? max(0, pos_lo - p.window + 1) / BN * BN : 0;
+    const int ns = min(p.num_splits, (pos_hi - win_tile) / p.split_len + 1);
+    const size_t row0 = (size_t)tu * p.num_splits * BM + r;  // piece s at row0 + s BM
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
     float M = -INFINITY;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-        const float m = s0 + lane < ns ? (s0 == 0 ? ml0.x : ml[2 * (s0 + lane)]) : -INFINITY;
-        M = fmaxf(M, m);
-    }
+    for (int s0 = 0; s0 < ns; s0 += 32)
+        if (s0 + lane < ns)
+            M = fmaxf(M, ml[row0 + (size_t)(s0 + lane) * BM].x);
 #pragma unroll
     for (int o = 16; o; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-
-    const float *po = p.part_o + (size_t)row * p.num_splits * D + lane * EPL;
     float acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; e++)
         acc[e] = 0.f;
     float L = 0.f;
     for (int s0 = 0; s0 < ns; s0 += 32) {
-        float w = 0.f;  // this lane's split weight 2^(m - M)
+        float w = 0.f;  // this lane's piece weight 2^(m - M)
         if (s0 + lane < ns) {
-            const float2 v = s0 == 0 ? ml0 : *reinterpret_cast<const float2 *>(ml + 2 * (s0 + lane));
-            w = exp2f(v.x - M);
-            L = fmaf(v.y, w, L);
+            const float2 v = ml[row0 + (size_t)(s0 + lane) * BM];
+            if (v.x != -INFINITY) {
+                w = exp2f(v.x - M);
+                L = fmaf(v.y, w, L);
+            }
         }
         const int n = min(32, ns - s0);
-        int s = 0;
-        for (; s + 4 <= n; s += 4) {
+        for (int s = 0; s < n; s += 4) {
             float v[4][EPL];
 #pragma unroll
             for (int u = 0; u < 4; u++) {
-                const float *src = po + (size_t)(s0 + s + u) * D;
-                if constexpr (EPL == 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(src);
-                    v[u][0] = x.x;
-                    v[u][1] = x.y;
-                    v[u][2] = x.z;
-                    v[u][3] = x.w;
-                } else {
-                    const float2 x = *reinterpret_cast<const float2 *>(src);
-                    v[u][0] = x.x;
-                    v[u][1] = x.y;
+                if (s + u < n) {
+                    const float *src = p.part_o + (row0 + (size_t)(s0 + s + u) * BM) * D + lane * EPL;
+                    if constexpr (EPL == 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(src);
+                        v[u][0] = x.x;
+                        v[u][1] = x.y;
+                        v[u][2] = x.z;
+                        v[u][3] = x.w;
+                    } else {
+                        const float2 x = *reinterpret_cast<const float2 *>(src);
+                        v[u][0] = x.x;
+                        v[u][1] = x.y;
+                    }
                 }
             }
 #pragma unroll
             for (int u = 0; u < 4; u++) {
-                const float ws = __shfl_sync(FULL, w, s + u);
+                const float ws = __shfl_sync(FULL, w, min(s + u, n - 1));
+                if (s + u < n) {
 #pragma unroll
-                for (int e = 0; e < EPL; e++)
-                    acc[e] = fmaf(v[u][e], ws, acc[e]);
+                    for (int e = 0; e < EPL; e++)
+                        acc[e] = fmaf(v[u][e], ws, acc[e]);
+                }
             }
-        }
-        for (; s < n; s++) {
-            const float ws = __shfl_sync(FULL, w, s);
-            const float *src = po + (size_t)(s0 + s) * D;
-#pragma unroll
-            for (int e = 0; e < EPL; e++)
-                acc[e] = fmaf(src[e], ws, acc[e]);
         }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1)
         L += __shfl_xor_sync(FULL, L, o);
-    const float inv = 1.0f / L;
-    bf16 *dst = p.out + (size_t)row * D + lane * EPL;
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    const size_t out_row = (size_t)(tok0 + r0 + (r >> pack_shift)) * p.H + hg * p.pack +
+                           (r & (p.pack - 1));
+    bf16 *dst = p.out + out_row * D + lane * EPL;
     float g[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; e++)
         g[e] = 1.0f;
     if ((p.flags & NA_OUT_GATE) && p.gate) {
-        const bf16 *gt = p.gate + (size_t)row * D + lane * EPL;
+        const bf16 *gt = p.gate + out_row * D + lane * EPL;
         uint32_t gw[EPL / 2];
         if constexpr (EPL == 4) {
             const uint2 u = __ldg(reinterpret_cast<const uint2 *>(gt));
@@ -865,16 +896,15 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
     });
     if (e != cudaSuccess)
         return e;
-    dim3 grid(p.q_tiles, p.H / p.pack, p.batch * p.num_splits);
+    const dim3 grid(p.full_units + p.tail_units * p.num_splits);
     e = p.softcap > 0.f ? launch_kernel(prefill_tc_kernel<D, true>, grid, dim3(THREADS), smem,
                                         stream, p, mq, mk, mv)
                         : launch_kernel(prefill_tc_kernel<D, false>, grid, dim3(THREADS), smem,
                                         stream, p, mq, mk, mv);
     if (e != cudaSuccess || p.num_splits == 1)
         return e;
-    const int nrows = total_tokens * p.H;
-    return launch_kernel(prefill_combine_kernel<D>, dim3((nrows + 7) / 8), dim3(256), 0, stream, p,
-                         total_tokens);
+    return launch_kernel(prefill_combine_kernel<D>, dim3(p.tail_units, BM / kMergeRows), dim3(256),
+                         0, stream, p);
 }
 
 }  // namespace

@@ -160,11 +160,19 @@ def test_zero_tokens_return_ok_without_launch(lib):
 
 
 def test_workspace_sizes_follow_the_plan(lib):
-    # long chunks fill the GPU: no key split, no workspace
-    assert na.na_prefill_workspace_size(na.AttnConfig(40, 8, 128, 64), 1, 2048, 2048, 32768) == 0
-    # a short chunk with long history splits the keys: (d + 2) floats per split row
+    # Whole units run one per CTA; only those left over after the last whole
+    # wave (152 SMs here and on the GB300) are cut, into up to 152 / leftover
+    # key ranges of at least four key tiles: 128 rows of (d + 2) floats each.
+    # 1024 tokens x 19 heads = 152 units: no leftover, no workspace.
+    assert na.na_prefill_workspace_size(na.AttnConfig(19, 19, 128), 1, 1024, 1024, 4096) == 0
+    # 2048 tokens x 40 heads = 640 units: 32 left over, cut in 4 (8192 keys each)
+    ws = na.na_prefill_workspace_size(na.AttnConfig(40, 8, 128, 64), 1, 2048, 2048, 32768)
+    assert ws == 32 * 4 * 128 * 130 * 4
+    # a short chunk with long history: all 32 units cut, in 4
     ws = na.na_prefill_workspace_size(na.AttnConfig(32, 8, 128), 1, 128, 128, 4096)
-    assert ws > 0 and ws % (128 * 32 * 130 * 4) == 0
+    assert ws == 32 * 4 * 128 * 130 * 4
+    # a short history cannot be cut into pieces of four key tiles: no workspace
+    assert na.na_prefill_workspace_size(na.AttnConfig(32, 8, 128), 1, 128, 128, 512) == 0
     # decode: one (d + 2)-float partial per head of each slice piece; pieces are
     # at most streams + grid, so the size follows the batch, not the lengths
     cfg = na.AttnConfig(32, 8, 128)
