@@ -154,7 +154,12 @@ PrefillPlan plan_prefill(const na_attn_cfg *c, int batch, int total_tokens, int 
     pl.q_tiles = (max_new_len + pl.tile_tokens - 1) / pl.tile_tokens;
     const long long units = (long long)batch * pl.q_tiles * (c->num_heads / pl.pack);
     const long long sms = sm_count();
-    pl.full_units = (int)(units >= sms ? units - units % sms : 0);
+    // With ragged lengths the unit count is only a bound (the shortest
+    // sequences' trailing units are empty), so the leftover units after the
+    // last whole wave are known to be real only when every sequence has
+    // max_new_len new tokens.
+    const bool exact = (long long)batch * max_new_len == total_tokens;
+    pl.full_units = (int)(units >= sms && exact ? units - units % sms : (units >= sms ? units : 0));
     pl.tail_units = (int)(units - pl.full_units);
     // Keys one tile can see: all history, or with a sliding window at most the
     // window plus the tile's own tokens (from the key tile holding the first
