@@ -11,9 +11,8 @@ visible keys) replayed as a CUDA graph.
 Also measured in the same line (`workloads`), each with its own roofline and
 its own CPU oracle baseline: the single-chunk 128-token parity workload (us
 and TFLOP/s), chunked prefill of 4096 tokens in 32 chunks of 128, single-token
-decode over 64 cached sequences (KV GB/s, with the importance pass and the
-decode with importance in one call), speculative pair verify, and the mixed
-varlen serving step.
+decode over 64 cached sequences (KV GB/s, with the importance pass),
+speculative pair verify, and the mixed varlen serving step.
 
 Timing: CUDA events on the launching stream around graph replays, W untimed
 warm-up replays, then K timed replays with the L2 flushed (a 256 MiB buffer
@@ -480,17 +479,9 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
     def importance():  # accumulated into a running per-key buffer
         na.na_decode_importance(cfg, probs, kv_lens, max_kv, imp, accumulate=True, status=status)
 
-    def fused():
-        na.na_attn_decode_imp(cfg, q_rot, cache, kv_lens, max_kv, out, probs, imp,
-                              accumulate=True, workspace=ws, status=status)
-
     def step():
         append()
         decode()
-
-    def step_fused():
-        append()
-        fused()
 
     for _ in range(warmup):
         step()
@@ -498,26 +489,16 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
     st = spread(time_graph(capture(step), steps, warmup, flush))
     kt = spread(time_graph(capture(decode), steps, warmup, flush))
     it = spread(time_graph(capture(importance), steps, warmup, flush))
-    ft = spread(time_graph(capture(step_fused), steps, warmup, flush))
-    fk = spread(time_graph(capture(fused), steps, warmup, flush))
     torch.cuda.synchronize()
     assert int(status.item()) == 0
 
     imp_bytes = sum(lens) * (H * 4 + 2 * 4)
-    fused_bytes = alg_bytes + sum(lens) * 2 * 4
     importance_rec = {
         "workload": "importance_" + wl.name, "metric": "importance GB/s", "unit": "GB/s",
         "value": imp_bytes / (it["median"] * 1e-3) / 1e9, "ms_per_step": it["median"],
         "ms_spread": it, "bytes_per_step": imp_bytes,
         "roofline": hbm_roofline(imp_bytes, it["median"], peaks, "na_decode_importance",
                                  traffic_from_profiles("importance.cu", "importance_" + wl.name))}
-    fused_rec = {
-        "workload": "decode_imp_" + wl.name, "metric": "decode+importance KV GB/s",
-        "unit": "GB/s", "value": (fused_bytes + append_bytes) / (ft["median"] * 1e-3) / 1e9,
-        "ms_per_step": ft["median"], "ms_spread": ft, "call_ms": fk, "bytes_per_step": fused_bytes,
-        "roofline": hbm_roofline(fused_bytes, fk["median"], peaks,
-                                 "na_attn_decode_imp (split pass + merge pass with importance)",
-                                 traffic_from_profiles("decode.cu", "decode_imp_" + wl.name))}
     return {"workload": wl.name, "metric": "decode KV GB/s", "unit": "GB/s",
             "value": (alg_bytes + append_bytes) / (st["median"] * 1e-3) / 1e9,
             "ms_per_step": st["median"], "ms_spread": st, "decode_call_ms": kt,
@@ -525,9 +506,7 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
             "roofline": hbm_roofline(alg_bytes, kt["median"], peaks,
                                      "na_attn_decode (split pass + combine)",
                                      traffic_from_profiles("decode.cu", wl.name)),
-            "importance": importance_rec, "fused": fused_rec,
-            "two_calls_vs_fused_ms": {"decode_plus_importance": kt["median"] + it["median"],
-                                      "decode_imp": fk["median"]}}
+            "importance": importance_rec}
 
 
 def bench_pair_verify(steps, warmup, peaks, flush):
@@ -792,9 +771,8 @@ def main(argv=None):
         extra.append(bench_chunked(W.C1, S, Wm, peaks, flush))
         extra.append(bench_chunked(W.C2, S, Wm, peaks, flush))
         dec_rec = bench_decode(W.C3, S, Wm, peaks, flush)
-        extra.append({k: v for k, v in dec_rec.items() if k not in ("importance", "fused")})
+        extra.append({k: v for k, v in dec_rec.items() if k != "importance"})
         extra.append(dec_rec["importance"])
-        extra.append(dec_rec["fused"])
         extra.append(bench_pair_verify(S, Wm, peaks, flush))
         extra.append(bench_varlen(W.C5, S, Wm, peaks, flush))
     torch.cuda.synchronize()

@@ -10,7 +10,8 @@ Entry points (same names as the C ABI):
   na_rope_append_kv      fused qk-norm + RoPE + KV-cache append
   na_attn_prefill_chunk  causal GQA attention of a chunk against the cache
   na_attn_decode         single-token decode with per-key probabilities
-  na_attn_decode_imp     the same, plus the step's importance (sum over heads)
+  na_decode_importance   the step's Born-rule importance (sum over heads of the probabilities)
+  na_attn_decode_static_ws  na_attn_decode with library-owned scratch
   na_prefill_workspace_size / na_decode_workspace_size / na_status_string
 """
 from __future__ import annotations
@@ -39,7 +40,7 @@ NA_RING_CACHE = 16
 
 # Every symbol include/na.h declares.
 EXPORTED = ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
-            "na_attn_decode_static_ws", "na_decode_importance", "na_attn_decode_imp",
+            "na_attn_decode_static_ws", "na_decode_importance",
             "na_prefill_workspace_size", "na_decode_workspace_size", "na_status_string",
             "na_selftest_wait_timeout")
 
@@ -92,15 +93,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.na_attn_decode_static_ws.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, I32, P,
                                              P]
     lib.na_decode_importance.argtypes = [cfgp, I32, P, I32, P, I32, P, I32, I32, P, P]
-    lib.na_attn_decode_imp.argtypes = [cfgp, I32, P, cachep, P, I32, P, P, P, I32, P, I32, I32,
-                                       I32, P, SZ, P, P]
     lib.na_prefill_workspace_size.argtypes = [cfgp, I32, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_decode_workspace_size.argtypes = [cfgp, I32, I32, I32, ctypes.POINTER(SZ)]
     lib.na_selftest_wait_timeout.argtypes = [P, P]
     lib.na_status_string.argtypes = [ctypes.c_int]
     lib.na_status_string.restype = ctypes.c_char_p
     for name in ("na_rope_append_kv", "na_attn_prefill_chunk", "na_attn_decode",
-                 "na_attn_decode_static_ws", "na_decode_importance", "na_attn_decode_imp",
+                 "na_attn_decode_static_ws", "na_decode_importance",
                  "na_prefill_workspace_size", "na_decode_workspace_size",
                  "na_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
@@ -270,23 +269,6 @@ def na_attn_decode(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: 
                             int(num_splits), _ptr(workspace), ws_bytes, _ptr(status),
                             _stream(stream))
     _check("na_attn_decode", rc)
-
-
-def na_attn_decode_imp(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: int, out,
-                       probs, imp, accumulate: bool = False, gate=None, workspace=None,
-                       num_splits: int = 0, status=None, stream=None):
-    """na_attn_decode plus the step's importance (sum over heads of the
-    probabilities) taken in the same merge pass; probs and imp are required."""
-    lib = load_library()
-    batch = int(q_rot.shape[0])
-    c, kc = cfg.c(), cache.c()
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.na_attn_decode_imp(ctypes.byref(c), batch, _ptr(q_rot), ctypes.byref(kc),
-                                _ptr(kv_lens), int(max_kv_len), _ptr(gate), _ptr(out), _ptr(probs),
-                                int(probs.shape[-1]), _ptr(imp), int(imp.shape[-1]),
-                                1 if accumulate else 0, int(num_splits), _ptr(workspace), ws_bytes,
-                                _ptr(status), _stream(stream))
-    _check("na_attn_decode_imp", rc)
 
 
 def na_attn_decode_static_ws(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: int,

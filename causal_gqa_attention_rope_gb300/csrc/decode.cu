@@ -754,195 +754,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
     }
 }
 
-// Merge pass that also sums the step's probabilities over heads (Born-rule
-// importance; cortiq-engine src/attention.rs, fn qwen_attention_core adds each
-// head's probabilities per key into `imp`).  One CTA per (sequence, 1024-key
-// range) covers every head: it reduces each head's pieces to (M, 1/L) with
-// merge_weights, as the per-head pass does, so outputs and probabilities are
-// bit-identical to it; rewrites the range's raw scores of every head as
-// probabilities; and adds them in head order (fp32, deterministic) into the
-// range's importance.  The sequence's output rows are shared out over its
-// range CTAs.  Per key the probabilities are read and written once and the
-// importance needs no second pass over them.
-constexpr int kMiThreads = 256;
-constexpr int kMiKeys = 4 * kMiThreads;
-
-template <int D>
-__global__ void __launch_bounds__(kMiThreads) decode_merge_imp_kernel(const DecodeParams p)
-{
-    extern __shared__ float mi_smem[];  // per head: M, 1/L, ok, first piece row, pieces
-    float *sM = mi_smem, *sInv = mi_smem + p.H;
-    int *sOk = reinterpret_cast<int *>(mi_smem + 2 * p.H);
-    int *sRow = sOk + p.H, *sNs = sOk + 2 * p.H;
-    grid_dependency_wait();
-    grid_dependents_launch();
-    const int b = blockIdx.y;
-    const int n = __ldg(p.kv_lens + b);
-    const bool lead = blockIdx.x == 0;  // also merges the output rows
-    bf16 *out = p.out + (size_t)b * p.H * D;
-    if (n <= 0 || (!(p.flags & NA_RING_CACHE) && n > p.capacity) || n > p.max_kv_len) {
-        if (lead) {
-            if (n != 0 && threadIdx.x == 0)
-                na_report(p.status, NA_ERR_CAPACITY);
-            for (int e = threadIdx.x; e < p.H * D; e += kMiThreads)
-                out[e] = __float2bfloat16_rn(0.f);
-        }
-        return;
-    }
-    const int k0 = blockIdx.x * kMiKeys;
-    if (k0 >= n)
-        return;  // the whole CTA is past the sequence
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hpc = p.group / p.head_chunks;
-
-    // This thread's four keys: with 16-byte rows four consecutive keys, else
-    // keys k0 + t, k0 + t + 256, ... (a warp touches whole lines either way).
-    const int kf = (p.window > 0 && n > p.window) ? n - p.window : 0;
-    const bool vrows = p.imp_vec != 0;
-    const int j0 = vrows ? k0 + 4 * (int)threadIdx.x : k0 + (int)threadIdx.x;
-    const int step = vrows ? 1 : kMiThreads;
-    const bool vec = vrows && j0 + 4 <= n;
-    float *base = p.probs + (size_t)b * p.H * p.probs_stride + j0;
-    // The first eight heads' raw scores are requested before the merge
-    // weights, so their latency overlaps it (in bounds whatever the pieces).
-    float4 x[8];
-    if (vec) {
-#pragma unroll
-        for (int u = 0; u < 8; u++)
-            if (u < p.H)
-                x[u] = *reinterpret_cast<const float4 *>(base + (size_t)u * p.probs_stride);
-    }
-
-    // Every head's (M, 1/L): a warp takes four heads at once, all their loads
-    // issued before the reductions (the arithmetic of merge_weights).
-    constexpr int HW = 4;
-    for (int hb = warp; hb < p.H; hb += (kMiThreads / 32) * HW) {
-        int first[HW], ns[HW], row0[HW];
-#pragma unroll
-        for (int q = 0; q < HW; q++) {
-            const int h = hb + q * (kMiThreads / 32);
-            first[q] = -1;
-            ns[q] = 0;
-            row0[q] = 0;
-            if (h < p.H) {
-                const int kvh = h / p.group, r = h - kvh * p.group;
-                const int stream = (b * p.KV + kvh) * p.head_chunks + r / hpc;
-                first[q] = p.piece_span[2 * stream];
-                const int last = p.piece_span[2 * stream + 1];
-                const bool ok = !(first[q] < 0 || last < first[q] || last >= p.max_pieces);
-                ns[q] = ok ? last - first[q] + 1 : -1;  // -1: the split pass gave up
-                row0[q] = ok ? first[q] * hpc + (r % hpc) : 0;
-            }
-        }
-        float m0[HW], l0[HW];
-#pragma unroll
-        for (int q = 0; q < HW; q++)
-            merge_lane_piece(p.part_ml + (size_t)row0[q] * 2, hpc, ns[q], lane, m0[q], l0[q]);
-#pragma unroll
-        for (int q = 0; q < HW; q++) {
-            const int h = hb + q * (kMiThreads / 32);
-            if (h >= p.H)
-                break;  // warp-uniform
-            bool ok = ns[q] >= 0;
-            float M = -INFINITY, inv_l = 0.f;
-            if (ok)
-                ok = merge_weights_from(m0[q], l0[q], p.part_ml + (size_t)row0[q] * 2, hpc, ns[q],
-                                        lane, M, inv_l);
-            if (!ok && lead && lane == 0)
-                na_report(p.status, NA_ERR_DEVICE_TIMEOUT);
-            if (lane == 0) {
-                sM[h] = M;
-                sInv[h] = inv_l;
-                sOk[h] = ok;
-                sRow[h] = row0[q];
-                sNs[h] = ok ? ns[q] : 0;
-            }
-        }
-    }
-    __syncthreads();
-
-    // Output rows: head h is merged by the sequence's range CTA h mod nr.
-    {
-        constexpr int EPL = D / 32;
-        const int nr = (n + kMiKeys - 1) / kMiKeys;  // range CTAs of this sequence
-        const bool gated = (p.flags & NA_OUT_GATE) && p.gate;
-        for (int h = blockIdx.x + nr * warp; h < p.H; h += nr * (kMiThreads / 32)) {
-            bf16 *orow = out + (size_t)h * D;
-            const bool ok = sOk[h];
-            const float *ml = p.part_ml + (size_t)sRow[h] * 2;
-            const float *po = p.part_o + (size_t)sRow[h] * D;
-#pragma unroll
-            for (int i = 0; i < EPL; i++) {
-                const int e = lane * EPL + i;
-                float o = 0.f;
-                if (ok) {
-                    o = merge_out_elem<D>(po, ml, hpc, sNs[h], e, sM[h], sInv[h]);
-                    if (gated)
-                        o = gated_elem(o, p.gate[((size_t)b * p.H + h) * D + e]);
-                }
-                orow[e] = __float2bfloat16_rn(o);
-            }
-        }
-    }
-
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (vec) {
-        for (int h0 = 0; h0 < p.H; h0 += 8) {
-            if (h0 > 0) {
-#pragma unroll
-                for (int u = 0; u < 8; u++)  // eight 16-byte loads in flight
-                    if (h0 + u < p.H)
-                        x[u] = *reinterpret_cast<const float4 *>(base + (size_t)(h0 + u) * p.probs_stride);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int h = h0 + u;
-                if (h < p.H && sOk[h]) {
-                    const float M = sM[h], inv_l = sInv[h];
-                    float4 y;
-                    y.x = prob_of(x[u].x, j0, kf, M, inv_l);
-                    y.y = prob_of(x[u].y, j0 + 1, kf, M, inv_l);
-                    y.z = prob_of(x[u].z, j0 + 2, kf, M, inv_l);
-                    y.w = prob_of(x[u].w, j0 + 3, kf, M, inv_l);
-                    *reinterpret_cast<float4 *>(base + (size_t)h * p.probs_stride) = y;
-                    acc[0] += y.x;
-                    acc[1] += y.y;
-                    acc[2] += y.z;
-                    acc[3] += y.w;
-                }
-            }
-        }
-        float4 *d4 = reinterpret_cast<float4 *>(p.imp + (size_t)b * p.imp_stride + j0);
-        float4 v = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        if (p.imp_accumulate) {
-            const float4 o = *d4;
-            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
-        }
-        *d4 = v;
-        return;
-    }
-    for (int h = 0; h < p.H; h++) {
-        if (!sOk[h])
-            continue;
-        const float M = sM[h], inv_l = sInv[h];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int j = j0 + k * step;
-            if (j < n) {
-                float *q = base + (size_t)h * p.probs_stride + k * step;
-                const float v = prob_of(*q, j, kf, M, inv_l);
-                *q = v;
-                acc[k] += v;
-            }
-        }
-    }
-    float *dst = p.imp + (size_t)b * p.imp_stride + j0;
-#pragma unroll
-    for (int k = 0; k < 4; k++)
-        if (j0 + k * step < n)
-            dst[k * step] = p.imp_accumulate ? dst[k * step] + acc[k] : acc[k];
-}
-
 template <int D, int HPC, bool CAPPED>
 cudaError_t launch_split(const DecodeParams &p, cudaStream_t stream)
 {
@@ -970,19 +781,12 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream)
                                     : launch_split<D, HPC, false>(p, stream);
     if (e != cudaSuccess)
         return e;
-    if (p.imp) {
-        const dim3 grid(max(1, (p.max_kv_len + kMiKeys - 1) / kMiKeys), p.batch);
-        return launch_kernel(decode_merge_imp_kernel<D>, grid, dim3(kMiThreads),
-                             decode_imp_smem_bytes(p.H), stream, p);
-    }
     return launch_kernel(decode_combine_kernel<D>, dim3(p.batch * p.H), dim3(256), 0, stream, p);
 }
 
 }  // namespace
 
 int decode_key_tile() { return DEC_TILE; }
-
-size_t decode_imp_smem_bytes(int H) { return (size_t)H * 5 * sizeof(float); }
 
 int decode_ctas_per_sm() { return 2; }
 

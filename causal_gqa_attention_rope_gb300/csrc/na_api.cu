@@ -10,10 +10,6 @@
 
 namespace {
 
-// Heads of the merge pass with importance: per-head values live in its dynamic
-// shared memory (5 words each, within the 48 KB default).
-constexpr int kMaxImpHeads = 2048;
-
 constexpr uint32_t kKnownFlags =
     NA_QK_NORM | NA_QK_NORM_ZERO_CENTERED | NA_V_NORM | NA_OUT_GATE | NA_RING_CACHE;
 constexpr double kPi = 3.14159265358979323846;
@@ -428,12 +424,11 @@ int na_decode_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t max_
     return NA_OK;
 }
 
-// Shared body of na_attn_decode and na_attn_decode_imp (imp == NULL: no importance).
-static int attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
-                       const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
-                       const void *gate, void *out, float *probs, int32_t probs_stride, float *imp,
-                       int32_t imp_stride, int32_t accumulate, int32_t num_splits, void *workspace,
-                       size_t ws_bytes, int32_t *status, void *stream)
+int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
+                   const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
+                   const void *gate, void *out, float *probs, int32_t probs_stride,
+                   int32_t num_splits, void *workspace, size_t ws_bytes, int32_t *status,
+                   void *stream)
 {
     int rc = check_cfg(cfg);
     if (rc != NA_OK)
@@ -486,45 +481,10 @@ static int attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     p.part_ml = p.part_o + rows * cfg->head_dim;
     p.piece_span = reinterpret_cast<int32_t *>(p.part_ml + rows * 2);
     p.status = status;
-    if (imp) {
-        p.imp = imp;
-        p.imp_stride = imp_stride;
-        p.imp_accumulate = accumulate ? 1 : 0;
-        p.imp_vec = aligned16(probs) && aligned16(imp) && probs_stride % 4 == 0 &&
-                    imp_stride % 4 == 0;
-    }
     return launch_decode(p, cfg->head_dim, pl.heads_per_cta, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? NA_OK
                : NA_ERR_CUDA;
-}
-
-int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
-                   const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
-                   const void *gate, void *out, float *probs, int32_t probs_stride,
-                   int32_t num_splits, void *workspace, size_t ws_bytes, int32_t *status,
-                   void *stream)
-{
-    return attn_decode(cfg, batch, q_rot, cache, kv_lens, max_kv_len, gate, out, probs,
-                       probs_stride, nullptr, 0, 0, num_splits, workspace, ws_bytes, status,
-                       stream);
-}
-
-int na_attn_decode_imp(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
-                       const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
-                       const void *gate, void *out, float *probs, int32_t probs_stride, float *imp,
-                       int32_t imp_stride, int32_t accumulate, int32_t num_splits, void *workspace,
-                       size_t ws_bytes, int32_t *status, void *stream)
-{
-    if (!probs || !imp)
-        return NA_ERR_INVALID_ARG;
-    if (cfg && cfg->num_heads > kMaxImpHeads)
-        return NA_ERR_UNSUPPORTED;
-    if (imp_stride < max_kv_len)
-        return NA_ERR_CAPACITY;
-    return attn_decode(cfg, batch, q_rot, cache, kv_lens, max_kv_len, gate, out, probs,
-                       probs_stride, imp, imp_stride, accumulate, num_splits, workspace, ws_bytes,
-                       status, stream);
 }
 
 }  // extern "C"

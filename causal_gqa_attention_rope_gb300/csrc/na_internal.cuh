@@ -252,10 +252,6 @@ struct DecodeParams {
     float *part_ml;            // [max_pieces][heads-per-CTA][2]  (max, sum) in the log2 domain
     int32_t *piece_span;       // [streams][2]  first and last piece id of each stream
     int32_t *status;
-    float *imp;                // [batch][imp_stride] or null: importance summed in the merge pass
-    long long imp_stride;
-    int imp_accumulate;        // add to imp instead of overwriting it
-    int imp_vec;               // probs and imp rows are 16-byte aligned (16-byte accesses)
 };
 
 struct PrefillParams {
@@ -303,7 +299,6 @@ cudaError_t launch_prefill(const PrefillParams &p, int d, int total_tokens, int 
                            cudaStream_t stream);
 size_t rope_append_smem_bytes(int H, int KV, int d, int rd);
 int decode_key_tile();
-size_t decode_imp_smem_bytes(int H);  // dynamic shared memory of the merge pass with importance
 int decode_ctas_per_sm();
 int prefill_key_tile();
 int prefill_q_tile();

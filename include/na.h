@@ -265,35 +265,6 @@ int na_decode_importance(const na_attn_cfg *cfg, int32_t batch, const float *pro
                          float *imp, int32_t imp_stride, int32_t accumulate, int32_t *status,
                          void *stream);
 
-/*
- * na_attn_decode and the step's Born-rule importance in one call, the sum over
- * heads taken in the merge pass that produces the probabilities.
- * [cortiq fn qwen_attention_core: the decode attends every head, then adds each
- *  head's probabilities per key into `imp`; fn attend_all_heads returns the sum.]
- *
- * Same arguments and results as na_attn_decode (out and probs are bit-identical
- * to what na_attn_decode writes for the same inputs and num_splits), plus
- *   imp[b][j] = sum over the H query heads of probs[b][h][j]     for j < kv_lens[b]
- * (accumulate != 0: imp[b][j] += that sum), summed in fp32 in head index order
- * (deterministic; it may differ from na_decode_importance in the last bits, which
- * groups the heads).  Keys past kv_lens[b] are not touched.  The probabilities
- * are read and written once: no second pass over them as with
- * na_attn_decode + na_decode_importance.
- *
- *   probs       required (not NULL), fp32 [batch][H][probs_stride].
- *   imp         fp32 [batch][imp_stride] (device), caller-owned.
- *   imp_stride  >= max_kv_len.  Strides a multiple of 4 with 16-byte-aligned probs
- *               and imp give 16-byte accesses; any stride is correct.
- * Errors: those of na_attn_decode; NA_ERR_INVALID_ARG for a NULL probs or imp;
- * NA_ERR_CAPACITY when imp_stride < max_kv_len; NA_ERR_UNSUPPORTED for more than
- * 2048 query heads.
- */
-int na_attn_decode_imp(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
-                       const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,
-                       const void *gate, void *out, float *probs, int32_t probs_stride, float *imp,
-                       int32_t imp_stride, int32_t accumulate, int32_t num_splits, void *workspace,
-                       size_t ws_bytes, int32_t *status, void *stream);
-
 /* Workspace bytes (HOST out-parameter) that na_attn_prefill_chunk needs for these bounds. */
 int na_prefill_workspace_size(const na_attn_cfg *cfg, int32_t batch, int32_t total_tokens,
                               int32_t max_new_len, int32_t max_total_len, size_t *bytes);

@@ -110,22 +110,6 @@ def test_capacity_and_workspace_checks(lib):
     assert rc == na.NA_ERR_INVALID_ARG
 
 
-def test_decode_with_importance_validated(lib):
-    """na_attn_decode_imp needs probs and imp, an imp stride covering the
-    longest sequence and at most 2048 heads; the decode's own checks follow."""
-    c = _cfg()
-    cache = na.na_kv_cache(16, 16, 2, 64)
-    call = lambda cfg, probs, ps, imp, istr, ws_bytes=1 << 20: lib.na_attn_decode_imp(
-        ctypes.byref(cfg), 2, 16, ctypes.byref(cache), 16, 40, None, 16, probs, ps, imp, istr, 0,
-        0, 16, ws_bytes, None, None)
-    assert call(c, None, 0, 16, 64) == na.NA_ERR_INVALID_ARG
-    assert call(c, 16, 64, None, 64) == na.NA_ERR_INVALID_ARG
-    assert call(c, 16, 64, 16, 32) == na.NA_ERR_CAPACITY
-    assert call(c, 16, 32, 16, 64) == na.NA_ERR_CAPACITY  # probability stride
-    assert call(_cfg(num_heads=4096, num_kv_heads=8), 16, 64, 16, 64) == na.NA_ERR_UNSUPPORTED
-    assert call(c, 16, 64, 16, 64, ws_bytes=8) == na.NA_ERR_WORKSPACE
-
-
 def test_wait_selftest_needs_a_status_word(lib):
     assert lib.na_selftest_wait_timeout(None, None) == na.NA_ERR_INVALID_ARG
 

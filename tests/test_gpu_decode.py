@@ -274,96 +274,3 @@ def test_calls_follow_the_current_stream(oracle):
     torch.cuda.synchronize()
     assert status == 0
     assert torch.equal(out, ref_out)
-
-
-# ------------------------------------ decode with importance in the merge pass --
-
-def _gpu_decode_imp(dec, probs_stride=None, imp_init=None, accumulate=False, num_splits=0):
-    import causal_gqa_attention_rope_gb300 as na
-    from harness import attn_cfg
-    dev = "cuda"
-    s = dec.spec
-    cfg = attn_cfg(s)
-    B = dec.q.shape[0]
-    max_kv = int(dec.kv_lens.max()) if B else 0
-    stride = probs_stride or max(max_kv, 1)
-    q = dec.q.to(dev)
-    cache = na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev))
-    kv = dec.kv_lens.to(dev)
-    gate = None if dec.gate is None else dec.gate.to(dev)
-    go = Guarded(q.shape, q.dtype, dev)
-    gp = Guarded((B, s.H, stride), torch.float32, dev, fill=-7.0)
-    gi = Guarded(tuple(imp_init.shape), torch.float32, dev, fill=imp_init.to(dev))
-    out, probs, imp = go.t, gp.t, gi.t
-    ws = na.workspace(na.na_decode_workspace_size(cfg, B, max_kv, num_splits), dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    na.na_attn_decode_imp(cfg, q, cache, kv, max_kv, out, probs, imp, accumulate=accumulate,
-                          gate=gate, workspace=ws, num_splits=num_splits, status=status)
-    torch.cuda.synchronize()
-    go.check("decode_imp out")
-    gp.check("decode_imp probs")
-    gi.check("decode_imp importance")
-    return out.cpu(), probs.cpu(), imp.cpu(), int(status.item())
-
-
-FUSED_IMP = {
-    # name: (spec, kv_lens, capacity, probs_stride, accumulate, num_splits)
-    "ragged_vec_rows": (W.Spec(H=8, KV=2, d=128, rd=128), [0, 1, 3, 700, 1500, 1027], 1536,
-                        1500, False, 0),
-    "odd_stride": (W.Spec(H=8, KV=2, d=128, rd=128), [0, 1, 3, 700, 1500, 1027], 1536, 1539,
-                   True, 0),
-    "window_gate_d64": (W.Spec(H=16, KV=4, d=64, rd=64, out_gate=True, window=200),
-                        [5, 64, 333, 2100], 2112, None, True, 0),
-    "softcap_forced_splits": (W.Spec(H=32, KV=8, d=128, rd=128, softcap=3.0),
-                              [77, 1024, 1025, 3000], 3072, 3072, False, 6),
-}
-
-
-@pytest.mark.parametrize("name", list(FUSED_IMP))
-def test_decode_with_importance(oracle, name):
-    """Outputs and probabilities are bit-identical to na_attn_decode's; the
-    importance matches the oracle's sum over heads (each probability is within
-    PROBS_MAX_ABS, so each sum within H times that); keys past kv_len untouched.
-    Rows of a multiple of 4 floats take the 16-byte path, the odd stride the
-    scalar one."""
-    from harness import PROBS_MAX_ABS
-    spec, lens, cap, stride, acc, splits = FUSED_IMP[name]
-    dec = W.make_decode(spec, lens, cap, seed=123)
-    ref_out, ref_probs, st = gpu_decode(dec, probs_stride=stride, num_splits=splits)
-    assert st == 0
-    B, H, pstride = ref_probs.shape
-    init = torch.rand((B, pstride), generator=torch.Generator().manual_seed(4))
-    out, probs, imp, st = _gpu_decode_imp(dec, probs_stride=stride, imp_init=init,
-                                          accumulate=acc, num_splits=splits)
-    assert st == 0
-    assert torch.equal(out, ref_out), "output differs from na_attn_decode"
-    assert torch.equal(probs, ref_probs), "probabilities differ from na_attn_decode"
-    _, ref_p = _oracle_decode(oracle, dec, stride=pstride)
-    ref = oracle.decode_importance(H, ref_p, dec.kv_lens.numpy(), imp=init.double().numpy(),
-                                   accumulate=acc)
-    for b, n in enumerate(lens):
-        err = float(np.max(np.abs(imp[b, :n].double().numpy() - ref[b, :n]))) if n else 0.0
-        assert err <= H * PROBS_MAX_ABS, f"importance b{b}: {err:.3e}"
-        assert torch.equal(imp[b, n:], init[b, n:]), "importance written past kv_len"
-
-
-def test_full_decode_with_importance_b64_h32kv8():
-    """The full decode workload through the fused call: outputs and
-    probabilities bit-identical to na_attn_decode, every sequence's importance
-    totals H, and it equals the fp32 head-order sum of the probabilities."""
-    dec = W.make_decode_workload(W.C3, seed=0)
-    B = dec.q.shape[0]
-    max_kv = int(dec.kv_lens.max())
-    stride = (max_kv + 3) // 4 * 4
-    ref_out, ref_probs, st = gpu_decode(dec, probs_stride=stride)
-    assert st == 0
-    out, probs, imp, st = _gpu_decode_imp(dec, probs_stride=stride, imp_init=torch.zeros(B, stride))
-    assert st == 0
-    assert torch.equal(out, ref_out) and torch.equal(probs, ref_probs)
-    H = probs.shape[1]
-    want = torch.zeros(B, stride)
-    for h in range(H):  # fp32, head order: the kernel's summation order
-        want += probs[:, h, :]
-    for b, n in enumerate(dec.kv_lens.tolist()):
-        assert abs(float(imp[b, :n].double().sum()) - H) < 1e-2, f"total b{b}"
-        assert torch.equal(imp[b, :n], want[b, :n]), f"importance b{b} is not the head-order sum"
