@@ -9,17 +9,21 @@
 // rope_rotate_scaled (half-split pairs (x[i], x[i + rd/2]), both outputs scaled
 // by the attention factor).
 //
-// One CTA per token; the kernel moves 2 * (H + 2 KV) * d * 2 bytes per token
-// and, at a few hundred tokens per call, is bound by the latency of that one
-// round trip.  So everything the token needs is requested first, and the work
-// between the loads and the stores is short and free of double precision:
-//   - rope_append_kernel (rotary_dim a multiple of 16): each thread owns one
-//     32-byte unit of a row -- chunks [8k, 8k + 8) and [rd/2 + 8k, ...) of the
-//     rotated part (eight rotation pairs), two consecutive chunks of the
-//     non-rotated tail, or of a V row -- loads it with two 16-byte loads, takes
-//     the row's sum of squares with shuffles among the row's lanes, rotates in
-//     registers and stores it with two 16-byte stores.  The only shared data
-//     are the cos/sin of the rd/2 pair indices, computed once per token.
+// The kernel moves 2 * (H + 2 KV) * d * 2 bytes per token and is bound by the
+// latency of its one round trip, so everything a thread needs is requested
+// first, the work between the loads and the stores is short and free of double
+// precision, and many small CTAs share an SM to overlap their round trips:
+//   - rope_append_kernel (rotary_dim a multiple of 16): a CTA of 64 threads
+//     takes 64 / (d / 16) rows of one token (grid: tokens x row groups); each
+//     thread owns one 32-byte unit of a row -- chunks [8k, 8k + 8) and
+//     [rd/2 + 8k, ...) of the rotated part (eight rotation pairs), two
+//     consecutive chunks of the non-rotated tail, or of a V row -- loads it
+//     with two 16-byte loads, takes the row's sum of squares with shuffles
+//     among the row's lanes, rotates in registers and stores it with two
+//     16-byte stores.  The only shared data are the cos/sin of the rd/2 pair
+//     indices, computed by the CTA (one 256-entry table lookup each, read
+//     through the cache).  One CTA per token of all rows left one CTA per SM
+//     and measured ~39 us per 2048-token chunk of 56 rows.
 //   - rope_append_staged_kernel (any even rotary_dim): the rows are staged in
 //     shared memory and every thread works on independent (row, pair) slots.
 //
@@ -299,17 +303,17 @@ __device__ __forceinline__ uint4 ldg_early(const void *p)
 
 // ------------------------------------------------------ register path --
 
-constexpr int kMaxUnits = 768;  // one unit per thread: up to 96 rows of d = 128
+constexpr int kAppendThreads = 64;  // one 32-byte row unit each: 4 rows of d = 128, 8 of d = 64
 
 template <int D>
-__global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppendParams p,
-                                                           const RopeTurns turns)
+__global__ void __launch_bounds__(kAppendThreads) rope_append_kernel(const RopeAppendParams p,
+                                                                const RopeTurns turns)
 {
     constexpr int UPR = D / 16;  // 32-byte units per row
-    __shared__ TrigEntry trig[256];
     __shared__ float4 cs[64];
     const int t = blockIdx.x;
     const int H = p.H, KV = p.KV, rows = H + 2 * KV;
+    const int row0 = blockIdx.y * (kAppendThreads / UPR);  // the CTA's first row
     const int half = p.rd / 2;
     const int lane = threadIdx.x & 31;
     const bool qk_norm = (p.flags & NA_QK_NORM) != 0;
@@ -318,8 +322,8 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
 
     // This thread's unit: row r, 8-element chunks starting at e0 and e1.
     const int unit = threadIdx.x;
-    const bool active = unit < rows * UPR;
-    const int r = unit / UPR, k = unit % UPR;
+    const int r = row0 + unit / UPR, k = unit % UPR;
+    const bool active = r < rows;
     const bool is_v = r >= H + KV;
     const bool rot = !is_v && k < p.rd / 16;
     int e0, e1;
@@ -334,10 +338,8 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
         e1 = e0 + 8;
     }
 
-    // Constant data and kernel parameters go before the wait: the table, and
-    // this thread's frequency (a dynamically indexed parameter).
-    for (int i = threadIdx.x; i < 256; i += blockDim.x)
-        reinterpret_cast<uint4 *>(trig)[i] = __ldg(reinterpret_cast<const uint4 *>(&kTrig) + i);
+    // Kernel parameters go before the wait: this thread's frequency (a
+    // dynamically indexed parameter).
     unsigned long long fhi = 0;
     unsigned int flo = 0;
     if ((int)threadIdx.x < half) {
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kMaxUnits) rope_append_kernel(const RopeAppend
     const int slot = ring ? pos % p.capacity : pos;
     __syncthreads();
     if ((int)threadIdx.x < half)  // stored [i][k] for pair 8k + i: a row's lanes read adjacent entries
-        cs[(threadIdx.x & 7) * 8 + (threadIdx.x >> 3)] = cos_sin_turns((unsigned)pos, fhi, flo, trig);
+        cs[(threadIdx.x & 7) * 8 + (threadIdx.x >> 3)] = cos_sin_turns((unsigned)pos, fhi, flo, kTrig.e);
     __syncthreads();
 
     float a[8], c[8];
@@ -583,16 +585,13 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, const double *inv_freq
     RopeTurns turns{};
     for (int i = 0; i < half && i < 64; i++)
         turns_fixed_point(inv_freq[i], turns.hi[i], turns.lo[i]);
-    const int units = (p.H + 2 * p.KV) * (p.d / 16);
-    if (p.rd % 16 == 0 && units <= kMaxUnits) {
-        int threads = (units + 31) / 32 * 32;
-        if (threads < 64)
-            threads = 64;
+    if (p.rd % 16 == 0) {
+        const int rows_per_cta = kAppendThreads / (p.d / 16);
+        const dim3 grid(p.total_tokens, (p.H + 2 * p.KV + rows_per_cta - 1) / rows_per_cta);
         if (p.d == 128)
-            return launch_kernel(rope_append_kernel<128>, dim3(p.total_tokens), dim3(threads), 0,
-                                 stream, p, turns);
-        return launch_kernel(rope_append_kernel<64>, dim3(p.total_tokens), dim3(threads), 0, stream,
-                             p, turns);
+            return launch_kernel(rope_append_kernel<128>, grid, dim3(kAppendThreads), 0, stream, p,
+                                 turns);
+        return launch_kernel(rope_append_kernel<64>, grid, dim3(kAppendThreads), 0, stream, p, turns);
     }
     const size_t smem = rope_append_smem_bytes(p.H, p.KV, p.d, p.rd);
     // the largest dynamic shared memory granted so far, per device
