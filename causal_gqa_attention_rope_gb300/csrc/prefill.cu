@@ -58,7 +58,7 @@ struct __align__(1024) TcSmem {
     uint64_t q_full;
     uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
     uint64_t s_full[NUM_S], s_free[NUM_S], p_full[NUM_S];
-    uint64_t o_done, drain[2];
+    uint64_t o_done[NUM_S], drain[2];  // o_done[b]: the PVs of tiles b, b + NUM_S, ...
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -85,6 +85,15 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, int32
 {
     if (!mbar_wait_bounded(bar, parity))
         na_report(status, NA_ERR_DEVICE_TIMEOUT);
+}
+
+// A bounded wait whose result every lane of the warp shares: the softmax warps
+// follow it with warp-collective tensor-memory loads and stores, which no lane
+// may skip while others execute them.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const int *abort_flag)
+{
+    const bool done = mbar_wait_bounded(bar, parity) && !aborted(abort_flag);
+    return __all_sync(0xffffffffu, done);
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c)
@@ -132,7 +141,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&sm.s_free[s], 1);
             mbar_init(&sm.p_full[s], 4);
         }
-        mbar_init(&sm.o_done, 1);
+        for (int s = 0; s < NUM_S; s++)
+            mbar_init(&sm.o_done[s], 1);
         mbar_init(&sm.drain[0], 1);
         mbar_init(&sm.drain[1], 1);
         sm.abort_flag = 0;
@@ -380,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc::mma_commit(&sm.s_free[sb]);
                 tc::mma_commit(&sm.v_empty[st]);
-                tc::mma_commit(&sm.o_done);
+                tc::mma_commit(&sm.o_done[sb]);
                 any = true;
             }
             if (!ok)
@@ -411,7 +421,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int sb = j % NUM_S;
             const int j0 = k_begin + j * BN;
             const uint32_t s_t = tmem + S_COL0 * (sb + 1) + lane_off;
-            if (!mbar_wait_bounded(&sm.s_full[sb], (j / NUM_S) & 1) || aborted(&sm.abort_flag)) {
+            if (!warp_wait(&sm.s_full[sb], (j / NUM_S) & 1, &sm.abort_flag)) {
                 ok = false;
                 break;
             }
@@ -488,7 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // Key rows past the valid range hold whatever the cache has there;
                 // zero them so P * V sees no non-finite values.
                 const int st = j % STAGES;
-                if (!mbar_wait_bounded(&sm.v_full[st], (j / STAGES) & 1)) {
+                if (!warp_wait(&sm.v_full[st], (j / STAGES) & 1, &sm.abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -503,14 +513,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc::fence_proxy_async_smem();
             }
-            // Wait for PV(j-1) on every tile: the parity wait is only exact while
-            // the waiter is at most one phase behind the barrier, and up to two
-            // PVs can be in flight here.
-            if (j >= 1 && !mbar_wait_bounded(&sm.o_done, (j - 1) & 1)) {
-                ok = false;
-                break;
-            }
+            // O is touched here only to rescale it (rare), and then PV(j-1) must
+            // have landed.  PV(j) commits to o_done[j % NUM_S], so a wait there is
+            // exact however rarely the softmax looks: the barrier's previous
+            // phase, PV(j-1-NUM_S), completed before S(j-1) could be issued (its
+            // S buffer had to be free), and its next one, PV(j-1+NUM_S), needs a
+            // P this warp has not written yet.  Waiting for PV(j-1) on every tile
+            // kept PV(j) from being queued behind it.
             if (j >= 1 && __any_sync(0xffffffffu, corr)) {
+                if (!warp_wait(&sm.o_done[(j - 1) % NUM_S], ((j - 1) / NUM_S) & 1, &sm.abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 // rescale this warp's O rows (PV(j-1) has landed)
                 tc::fence_after_sync();
                 const float a = corr ? alpha : 1.f;
@@ -561,7 +575,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) {
             if (lane == 0)
                 set_abort(&sm.abort_flag, p.status);
-        } else if (mbar_wait_bounded(&sm.o_done, (n_tiles - 1) & 1)) {
+        } else if (warp_wait(&sm.o_done[(n_tiles - 1) % NUM_S], ((n_tiles - 1) / NUM_S) & 1,
+                             &sm.abort_flag)) {
             // ---------------------------------------------------- epilogue --
             // Each thread writes its O row (normalised unless this is a split
             // partial) into the idle K ring, rows padded by 16 bytes so the
