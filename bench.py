@@ -361,19 +361,43 @@ def bench_chunked(wl: W.PrefillWorkload, steps: int, warmup: int, peaks, flush,
                                        "replayed)", traffic_from_profiles("prefill.cu", wl.name))}
 
     if with_e2e:
+        # The step through the public API with host buffers, pipelined as a
+        # serving loop would: chunk c's Q/K/V are copied in on one stream and
+        # its output copied back on another, so the copies of other chunks
+        # overlap the kernels of chunk c.  Every byte crosses inside the timed
+        # region: it opens before the first copy-in and closes after the last
+        # copy-out.
         hq, hk, hv = (x.pin_memory() for x in (prompt.q[0], prompt.k[0], prompt.v[0]))
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        comp = torch.cuda.current_stream()
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
         e2e = []
         for i in range(max(1, steps // 2) + 1):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            run_step()
-            hout.copy_(out, non_blocking=True)
-            b.record()
+            a.record(comp)
+            h2d.wait_event(a)
+            ins = []
+            with torch.cuda.stream(h2d):
+                for (lo, hi, n, cu, lens, views) in chunks:
+                    q[lo:hi].copy_(hq[lo:hi], non_blocking=True)
+                    k[lo:hi].copy_(hk[lo:hi], non_blocking=True)
+                    v[lo:hi].copy_(hv[lo:hi], non_blocking=True)
+                    e = ev()
+                    e.record(h2d)
+                    ins.append(e)
+            for c, (lo, hi, n, cu, lens, views) in enumerate(chunks):
+                comp.wait_event(ins[c])
+                append(c)
+                attend(c)
+                e = ev()
+                e.record(comp)
+                d2h.wait_event(e)
+                with torch.cuda.stream(d2h):
+                    hout[lo:hi].copy_(out[lo:hi], non_blocking=True)
+            comp.wait_stream(d2h)
+            b.record(comp)
             torch.cuda.synchronize()
             if i > 0:  # the first is a warm-up of the host path
                 e2e.append(a.elapsed_time(b))
@@ -382,8 +406,10 @@ def bench_chunked(wl: W.PrefillWorkload, steps: int, warmup: int, peaks, flush,
                       "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hq, hk, hv)),
                       "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                       "ms_per_step": es["median"], "ms_spread": es,
-                      "api": "na_rope_append_kv + na_attn_prefill_chunk per chunk, eager, pinned "
-                             "host inputs copied in and the output copied out each step"}
+                      "api": "na_rope_append_kv + na_attn_prefill_chunk per chunk, eager; each "
+                             "chunk's Q/K/V copied in from pinned host memory on a copy stream "
+                             "and its output copied back on another, overlapping the kernels of "
+                             "the other chunks; all copies inside the timed region"}
     return res
 
 
