@@ -731,6 +731,35 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
     const int tu = blockIdx.x;
+    const int r = blockIdx.y * kMergeRows + warp;            // the warp's row of the unit
+    const size_t row0 = (size_t)tu * p.num_splits * BM + r;  // piece s at row0 + s BM
+    // The pieces' (max, sum) (lane s: piece s) and rows of the first four
+    // pieces are requested at once, in parallel with the sequence bounds: one
+    // round trip instead of three dependent ones.  Pieces past the row's last
+    // one are read but never used (their slots hold other calls' rows).
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
+    float2 ml_pre = make_float2(-INFINITY, 0.f);
+    if (lane < p.num_splits)
+        ml_pre = ml[row0 + (size_t)lane * BM];
+    auto load_row = [&](int s, float (&v)[EPL]) {
+        const float *src = p.part_o + (row0 + (size_t)s * BM) * D + lane * EPL;
+        if constexpr (EPL == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src);
+            v[0] = x.x;
+            v[1] = x.y;
+            v[2] = x.z;
+            v[3] = x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2 *>(src);
+            v[0] = x.x;
+            v[1] = x.y;
+        }
+    };
+    float pre[4][EPL];
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+        if (u < p.num_splits)
+            load_row(u, pre[u]);
     const int unit = p.full_units + tu;
     const int hg = (unit / p.q_tiles) % p.HG;
     const int slot = unit / (p.q_tiles * p.HG);
@@ -746,19 +775,30 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     if (prior < 0 || (!ring && pos_hi >= p.capacity) || pos_hi >= p.max_total_len)
         return;
     const int pack_shift = __ffs(p.pack) - 1;
-    const int r = blockIdx.y * kMergeRows + warp;
     if (r >= (rows_tok << pack_shift))
         return;
+    const size_t out_row = (size_t)(tok0 + r0 + (r >> pack_shift)) * p.H + hg * p.pack +
+                           (r & (p.pack - 1));
+    uint32_t gw[EPL / 2];  // gate words, requested before the merge arithmetic
+    const bool gated = (p.flags & NA_OUT_GATE) && p.gate;
+    if (gated) {
+        const bf16 *gt = p.gate + out_row * D + lane * EPL;
+        if constexpr (EPL == 4) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(gt));
+            gw[0] = u.x;
+            gw[1] = u.y;
+        } else {
+            gw[0] = __ldg(reinterpret_cast<const unsigned int *>(gt));
+        }
+    }
     // pieces with keys: the splits start at the key tile holding the first
     // row's window start (0 without a window), split_len keys apart
     const int win_tile = p.window > 0 ? max(0, pos_lo - p.window + 1) / BN * BN : 0;
     const int ns = min(p.num_splits, (pos_hi - win_tile) / p.split_len + 1);
-    const size_t row0 = (size_t)tu * p.num_splits * BM + r;  // piece s at row0 + s BM
-    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
     float M = -INFINITY;
     for (int s0 = 0; s0 < ns; s0 += 32)
         if (s0 + lane < ns)
-            M = fmaxf(M, ml[row0 + (size_t)(s0 + lane) * BM].x);
+            M = fmaxf(M, s0 == 0 ? ml_pre.x : ml[row0 + (size_t)(s0 + lane) * BM].x);
 #pragma unroll
     for (int o = 16; o; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
@@ -770,7 +810,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     for (int s0 = 0; s0 < ns; s0 += 32) {
         float w = 0.f;  // this lane's piece weight 2^(m - M)
         if (s0 + lane < ns) {
-            const float2 v = ml[row0 + (size_t)(s0 + lane) * BM];
+            const float2 v = s0 == 0 ? ml_pre : ml[row0 + (size_t)(s0 + lane) * BM];
             if (v.x != -INFINITY) {
                 w = exp2f(v.x - M);
                 L = fmaf(v.y, w, L);
@@ -781,19 +821,12 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
             float v[4][EPL];
 #pragma unroll
             for (int u = 0; u < 4; u++) {
-                if (s + u < n) {
-                    const float *src = p.part_o + (row0 + (size_t)(s0 + s + u) * BM) * D + lane * EPL;
-                    if constexpr (EPL == 4) {
-                        const float4 x = *reinterpret_cast<const float4 *>(src);
-                        v[u][0] = x.x;
-                        v[u][1] = x.y;
-                        v[u][2] = x.z;
-                        v[u][3] = x.w;
-                    } else {
-                        const float2 x = *reinterpret_cast<const float2 *>(src);
-                        v[u][0] = x.x;
-                        v[u][1] = x.y;
-                    }
+                if (s0 + s == 0) {
+#pragma unroll
+                    for (int e = 0; e < EPL; e++)
+                        v[u][e] = pre[u][e];
+                } else if (s + u < n) {
+                    load_row(s0 + s + u, v[u]);
                 }
             }
 #pragma unroll
@@ -811,23 +844,12 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     for (int o = 16; o; o >>= 1)
         L += __shfl_xor_sync(FULL, L, o);
     const float inv = L > 0.f ? 1.0f / L : 0.f;
-    const size_t out_row = (size_t)(tok0 + r0 + (r >> pack_shift)) * p.H + hg * p.pack +
-                           (r & (p.pack - 1));
     bf16 *dst = p.out + out_row * D + lane * EPL;
     float g[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; e++)
         g[e] = 1.0f;
-    if ((p.flags & NA_OUT_GATE) && p.gate) {
-        const bf16 *gt = p.gate + out_row * D + lane * EPL;
-        uint32_t gw[EPL / 2];
-        if constexpr (EPL == 4) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(gt));
-            gw[0] = u.x;
-            gw[1] = u.y;
-        } else {
-            gw[0] = __ldg(reinterpret_cast<const unsigned int *>(gt));
-        }
+    if (gated) {
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) {
             g[e] = __fdividef(1.0f, 1.0f + __expf(-__uint_as_float(gw[e / 2] << 16)));
