@@ -203,7 +203,9 @@ DecodePlan plan_decode(const na_attn_cfg *c, int batch, int max_kv_len, int num_
     DecodePlan pl{};
     const int tile = decode_key_tile();
     const int group = c->num_heads / c->num_kv_heads;
-    pl.heads_per_cta = (group % 4 == 0) ? 4 : ((group % 2 == 0) ? 2 : 1);
+    // query heads scored together (the MMA takes up to 8): each stream of
+    // K/V is read once for them
+    pl.heads_per_cta = (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : ((group % 2 == 0) ? 2 : 1);
     const int len = max_kv_len > 0 ? max_kv_len : 1;
     int min_slice = num_splits > 0 ? (len + num_splits - 1) / num_splits : 4 * tile;
     if (min_slice < 1)
@@ -360,6 +362,7 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
     p.tile_tokens = pl.tile_tokens;
     p.q_tiles = pl.q_tiles;
     p.HG = p.H / pl.pack;
+    p.kv_read_once = (pl.q_tiles == 1 && p.HG == p.KV) ? 1 : 0;
     p.full_units = pl.full_units;
     p.tail_units = pl.tail_units;
     p.split_len = pl.split_len;
@@ -441,6 +444,9 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
         return NA_ERR_INVALID_ARG;
     if ((cfg->flags & NA_RING_CACHE) ? cfg->window > cache->capacity : max_kv_len > cache->capacity)
         return NA_ERR_CAPACITY;
+    // a ring is read in whole key tiles, which must not cross its end
+    if ((cfg->flags & NA_RING_CACHE) && cache->capacity % decode_key_tile() != 0)
+        return NA_ERR_UNSUPPORTED;
     if (probs && probs_stride < max_kv_len)
         return NA_ERR_CAPACITY;
     const bool gated = (cfg->flags & NA_OUT_GATE) != 0;
@@ -456,6 +462,7 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     p.group = p.H / p.KV;
     p.batch = batch;
     p.capacity = cache->capacity;
+    p.cache_batch = cache->batch;
     p.scale_log2 = score_scale_log2(cfg);
     p.head_chunks = p.group / pl.heads_per_cta;
     p.grid = pl.grid;

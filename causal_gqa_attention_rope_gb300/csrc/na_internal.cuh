@@ -234,6 +234,7 @@ struct RopeAppendParams {
 
 struct DecodeParams {
     int H, KV, group, batch, capacity;
+    int cache_batch;           // sequences the cache holds (rows of the tensor maps)
     float scale_log2;          // score scale * log2(e)
     int head_chunks;           // group / heads-per-CTA
     int grid;                  // CTAs of the split pass, one key slice each
@@ -270,6 +271,7 @@ struct PrefillParams {
     int tail_units;            // the units after them, each cut into num_splits key ranges
     int split_len;             // keys per piece of a cut unit (multiple of the key tile)
     int num_splits;            // pieces per cut unit (1: the tail units run whole too)
+    int kv_read_once;          // every K/V tile is read by one CTA only (L2 evict-first loads)
     uint32_t flags;
     const int32_t *cu_seqlens, *cache_lens;
     const bf16 *q, *cache_k, *cache_v, *gate;

@@ -205,6 +205,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         prior = __shfl_sync(0xffffffffu, pl, src);
     }
     const int spec_row = (b * p.KV + kvh) * p.capacity + split_off;  // tile 0 without a window
+    // K/V tiles that no other CTA of the call reads (one query tile holding
+    // every query head of its kv group) are loaded first in line for L2
+    // eviction, so streaming them does not push out lines worth keeping.
+    const bool read_once = p.kv_read_once != 0;
+    const uint64_t kv_policy = l2_policy_evict_first();
+    auto load_kv = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+        if (read_once)
+            tc::tma_load_2d_hint(dst, map, x, y, bar, kv_policy);
+        else
+            tc::tma_load_2d(dst, map, x, y, bar);
+    };
     // With a single sequence the first K and V tiles depend only on the block,
     // and its tokens start at row 0: those copies are issued before the
     // sequence bounds arrive, overlapping that round trip (a CTA that turns out
@@ -216,10 +227,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc::tma_load_3d(sm.q[kb], &map_q, kb * 64, h0, r0, &sm.q_full);
         mbar_arrive_expect_tx(&sm.k_full[0], KB * BN * 128);
         for (int kb = 0; kb < KB; kb++)
-            tc::tma_load_2d(sm.k[0][kb], &map_k, kb * 64, spec_row, &sm.k_full[0]);
+            load_kv(sm.k[0][kb], &map_k, kb * 64, spec_row, &sm.k_full[0]);
         mbar_arrive_expect_tx(&sm.v_full[0], KB * BN * 128);
         for (int kb = 0; kb < KB; kb++)
-            tc::tma_load_2d(sm.v[0][kb], &map_v, kb * 64, spec_row, &sm.v_full[0]);
+            load_kv(sm.v[0][kb], &map_v, kb * 64, spec_row, &sm.v_full[0]);
     }
     if (!(p.batch > 1 && p.batch <= 32)) {
         tok0 = __ldg(p.cu_seqlens + b);
@@ -293,10 +304,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = eager ? 1 : 0; j < pre; j++) {
             mbar_arrive_expect_tx(&sm.k_full[j], KB * BN * 128);
             for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_2d(sm.k[j][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[j]);
+                load_kv(sm.k[j][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[j]);
             mbar_arrive_expect_tx(&sm.v_full[j], KB * BN * 128);
             for (int kb = 0; kb < KB; kb++)
-                tc::tma_load_2d(sm.v[j][kb], &map_v, kb * 64, tile_row(j), &sm.v_full[j]);
+                load_kv(sm.v[j][kb], &map_v, kb * 64, tile_row(j), &sm.v_full[j]);
         }
     }
     tc::fence_before_sync();
@@ -317,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mbar_arrive_expect_tx(&sm.k_full[st], KB * BN * 128);
                 for (int kb = 0; kb < KB; kb++)
-                    tc::tma_load_2d(sm.k[st][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[st]);
+                    load_kv(sm.k[st][kb], &map_k, kb * 64, tile_row(j), &sm.k_full[st]);
                 if (!mbar_wait_bounded(&sm.v_empty[st], par) || aborted(&sm.abort_flag)) {
                     set_abort(&sm.abort_flag, p.status);
                     drain_wait(&sm.k_full[st], (j / STAGES) & 1, p.status);
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 mbar_arrive_expect_tx(&sm.v_full[st], KB * BN * 128);
                 for (int kb = 0; kb < KB; kb++)
-                    tc::tma_load_2d(sm.v[st][kb], &map_v, kb * 64, tile_row(j), &sm.v_full[st]);
+                    load_kv(sm.v[st][kb], &map_v, kb * 64, tile_row(j), &sm.v_full[st]);
                 issued = j + 1;
             }
             // every copy issued lands before the CTA can exit
@@ -866,40 +877,6 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
         *reinterpret_cast<uint32_t *>(dst) = packed[0];
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-// bf16 tensor map with 64-element (128-byte) inner boxes and 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-              const cuuint64_t *strides_bytes, const cuuint32_t *box)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (!fn)
-        return false;
-    const cuuint32_t es[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
-              dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache_batch,
                              cudaStream_t stream)
@@ -909,7 +886,7 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)total_tokens};
         const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.H * D * 2};
         const cuuint32_t box[3] = {64, (cuuint32_t)p.pack, (cuuint32_t)p.tile_tokens};
-        if (!make_map(&mq, p.q, 3, dims, strides, box))
+        if (!make_bf16_tile_map(&mq, p.q, 3, dims, strides, box))
             return cudaErrorInvalidValue;
     }
     {
@@ -917,8 +894,8 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
         const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
         const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
         const cuuint32_t box[2] = {64, BN};
-        if (!make_map(&mk, p.cache_k, 2, dims, strides, box) ||
-            !make_map(&mv, p.cache_v, 2, dims, strides, box))
+        if (!make_bf16_tile_map(&mk, p.cache_k, 2, dims, strides, box) ||
+            !make_bf16_tile_map(&mv, p.cache_v, 2, dims, strides, box))
             return cudaErrorInvalidValue;
     }
     const size_t smem = tc_smem_bytes<D>();
@@ -945,6 +922,40 @@ cudaError_t launch_prefill_t(const PrefillParams &p, int total_tokens, int cache
 }
 
 }  // namespace
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 64-element (128-byte) inner boxes and 128-byte swizzle.
+bool make_bf16_tile_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides_bytes, const cuuint32_t *box)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+              dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int prefill_key_tile() { return BN; }
 int prefill_q_tile() { return BM; }

@@ -177,6 +177,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
 
 // ------------------------------------------------------------------- TMA --
 
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar)
 {
@@ -184,6 +185,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// The same with an L2 cache policy (from createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                 uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
@@ -209,3 +221,9 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 }
 
 }  // namespace tc
+
+// Host: a bf16 tensor map of the given rank (dims innermost first, byte strides
+// of the outer dims) with 64-element (128-byte) inner boxes and 128-byte
+// swizzle; false when the driver rejects it.
+bool make_bf16_tile_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                        const cuuint64_t *strides_bytes, const cuuint32_t *box);

@@ -63,7 +63,8 @@ typedef enum na_status {
                                          per sequence) - 1 positions, so a whole chunk is written first
                                          without overwriting a key any of its rows still reads.
                                          Prefill needs capacity % 128 == 0 and capacity >= window +
-                                         max_new_len - 1; decode needs capacity >= window. */
+                                         max_new_len - 1; decode needs capacity >= window and
+                                         capacity % 64 == 0 (NA_ERR_UNSUPPORTED otherwise). */
 
 /* One attention layer [cortiq struct QwenAttnCfg, the in-scope fields]. */
 typedef struct na_attn_cfg {
@@ -199,6 +200,11 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
  *              capacity or max_kv_len (zero output), NA_ERR_DEVICE_TIMEOUT when
  *              a wait of the split pass gave up (the affected heads get a zero
  *              output and no probabilities).
+ * Errors (before anything is enqueued): NA_ERR_INVALID_ARG for null or
+ * misaligned buffers, NA_ERR_CAPACITY when max_kv_len (or, with a ring, the
+ * window) exceeds the capacity or a stride, NA_ERR_UNSUPPORTED for a ring whose
+ * capacity is not a multiple of 64 (keys are read in aligned 64-key tiles),
+ * NA_ERR_WORKSPACE for a missing or short workspace.
  */
 int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
                    const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,

@@ -170,7 +170,8 @@ def test_workspace_sizes_follow_the_plan(lib):
 
 def test_ring_cache_capacity_rules(lib):
     """A ring cache needs whole 128-key tiles and room for a window plus a chunk
-    in prefill, and at least a window in decode (checked before any launch)."""
+    in prefill, and at least a window in whole 64-key tiles in decode (checked
+    before any launch)."""
     c = _cfg(window=200, ring_cache=True)
     odd = na.na_kv_cache(16, 16, 1, 200)       # not a multiple of 128
     rc = lib.na_attn_prefill_chunk(ctypes.byref(c), 1, 16, 16, 10, 10, 5000, 16,
@@ -183,6 +184,10 @@ def test_ring_cache_capacity_rules(lib):
     rc = lib.na_attn_decode(ctypes.byref(c), 1, 16, ctypes.byref(small), 16, 5000, None, 16,
                             None, 0, 0, 16, 1 << 30, None, None)
     assert rc == na.NA_ERR_CAPACITY            # window 200 > 128 slots
+    ring200 = na.na_kv_cache(16, 16, 1, 200)   # holds the window, not a multiple of 64
+    rc = lib.na_attn_decode(ctypes.byref(c), 1, 16, ctypes.byref(ring200), 16, 5000, None, 16,
+                            None, 0, 0, 16, 1 << 30, None, None)
+    assert rc == na.NA_ERR_UNSUPPORTED         # decode reads the ring in whole 64-key tiles
 
 
 def test_no_fallback_without_the_library(tmp_path, monkeypatch):

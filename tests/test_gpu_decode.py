@@ -40,6 +40,8 @@ SHAPES = {
     "h10kv2d128_group5": W.Spec(H=10, KV=2, d=128, rd=128),
     "h16kv2d64_group8_gate": W.Spec(H=16, KV=2, d=64, rd=64, out_gate=True),
     "h4kv2d128_group2_scale": W.Spec(H=4, KV=2, d=128, rd=128, sm_scale=0.2),
+    "h16kv2d128_group8": W.Spec(H=16, KV=2, d=128, rd=128),        # 8 heads per MMA
+    "h32kv2d128_group16_softcap": W.Spec(H=32, KV=2, d=128, rd=128, softcap=30.0),  # 2 head chunks
 }
 
 
