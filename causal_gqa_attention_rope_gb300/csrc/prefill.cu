@@ -315,6 +315,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
 
+    // Output rows are staged in shared memory by the softmax warps (they hold
+    // the tensor-memory lanes) and then stored by all eight warps, SR rows
+    // each: one warp per sub-partition storing 32 rows back to back was
+    // latency-bound (~1.5 us per CTA, 3.3 us with the gate).  A warp's gate
+    // words for its rows are requested early -- warps 0-3 now, the softmax
+    // warps after their last tile.
+    constexpr int LDS = D + 4;   // staged row stride (floats): conflict-free row writes
+    constexpr int EPL = D / 32;  // elements per lane in the row stores
+    constexpr int GW = D / 64;   // 32-bit words of gate per lane and row
+    constexpr int SR = BM / 8;   // rows stored per warp
+    float *stage = reinterpret_cast<float *>(&sm.k[0][0][0]);  // the K ring, idle by then
+    const bool split_out = nsplit > 1;
+    // rows of this piece in the workspace: [tail unit][split][row]
+    const size_t piece_row0 = ((size_t)tail_unit * p.num_splits + split) * BM;
+    const bool gated_out = !split_out && (p.flags & NA_OUT_GATE) && p.gate;
+    uint32_t gq[SR][GW];
+    auto load_gate = [&]() {
+#pragma unroll
+        for (int i = 0; i < SR; i++) {
+            const int rr = warp * SR + i;
+            const size_t off = ((size_t)(tok0 + r0 + (rr >> pack_shift)) * p.H + h0 +
+                                (rr & (p.pack - 1))) * D + lane * 2 * GW;
+            gq[i][0] = 0;
+            if constexpr (GW == 2)
+                gq[i][1] = 0;
+            if (rr < rows) {
+                if constexpr (GW == 2) {
+                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p.gate + off));
+                    gq[i][0] = u.x;
+                    gq[i][1] = u.y;
+                } else {
+                    gq[i][0] = __ldg(reinterpret_cast<const unsigned int *>(p.gate + off));
+                }
+            }
+        }
+    };
+    if (warp < 4 && gated_out)
+        load_gate();
+
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
@@ -557,32 +596,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0)
                 mbar_arrive(&sm.p_full[sb]);
         }
-        // Gate values of this lane's slice of the warp's 32 output rows, all
-        // requested now so their latency overlaps the last P V product
-        // (loaded one row at a time they cost ~25 us per CTA).
-        constexpr int GW = D / 64;  // 32-bit words of gate per lane and row
-        const bool gated = ok && nsplit == 1 && (p.flags & NA_OUT_GATE) && p.gate;
-        uint32_t gpre[32][GW];
-        if (gated) {
-#pragma unroll
-            for (int i = 0; i < 32; i++) {
-                const int rr = quarter * 32 + i;
-                const size_t off = ((size_t)(tok0 + r0 + (rr >> pack_shift)) * p.H + h0 +
-                                    (rr & (p.pack - 1))) * D + lane * 2 * GW;
-                gpre[i][0] = 0;
-                if constexpr (GW == 2)
-                    gpre[i][1] = 0;
-                if (rr < rows) {
-                    if constexpr (GW == 2) {
-                        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p.gate + off));
-                        gpre[i][0] = u.x;
-                        gpre[i][1] = u.y;
-                    } else {
-                        gpre[i][0] = __ldg(reinterpret_cast<const unsigned int *>(p.gate + off));
-                    }
-                }
-            }
-        }
+        // This warp's gate rows, requested now so their latency overlaps the
+        // last P V product.
+        if (ok && gated_out)
+            load_gate();
         if (!ok) {
             if (lane == 0)
                 set_abort(&sm.abort_flag, p.status);
@@ -594,12 +611,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             // row-per-thread writes are bank-conflict free; then each warp
             // stores its 32 rows one row per instruction, coalesced.
             tc::fence_after_sync();
-            constexpr int LDS = D + 4;
-            constexpr int EPL = D / 32;  // elements per lane in the row stores
-            float *stage = reinterpret_cast<float *>(&sm.k[0][0][0]);
-            const bool split_out = nsplit > 1;
-            // rows of this piece in the workspace: [tail unit][split][row]
-            const size_t piece_row0 = ((size_t)tail_unit * p.num_splits + split) * BM;
             const float scale = split_out ? 1.0f : (l > 0.f ? 1.0f / l : 0.f);
             {
                 uint32_t o[D / 32][32];  // the whole row in one round of loads
@@ -622,69 +633,63 @@ __global__ void __launch_bounds__(THREADS, 1)
                 p.part_ml[(piece_row0 + r) * 2] = m_ref;
                 p.part_ml[(piece_row0 + r) * 2 + 1] = l;
             }
-            __syncwarp();
-            // One row per step, lanes across the row.
-            auto row_out = [&](int i, const uint32_t *gw) {
-                const int rr = quarter * 32 + i;
-                const size_t tok = (size_t)(tok0 + r0 + (rr >> pack_shift));
-                const int h = h0 + (rr & (p.pack - 1));
-                const float *src = stage + rr * LDS + lane * EPL;
-                float v[EPL];
-                if constexpr (EPL == 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(src);
-                    v[0] = x.x;
-                    v[1] = x.y;
-                    v[2] = x.z;
-                    v[3] = x.w;
-                } else {
-                    const float2 x = *reinterpret_cast<const float2 *>(src);
-                    v[0] = x.x;
-                    v[1] = x.y;
-                }
-                if (split_out) {
-                    float *dst = p.part_o + (piece_row0 + rr) * D + lane * EPL;
-                    if constexpr (EPL == 4)
-                        *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-                    else
-                        *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
-                    return;
-                }
-                if (gw) {
-#pragma unroll
-                    for (int e = 0; e < EPL; e += 2) {
-                        const float g0 = __uint_as_float(gw[e / 2] << 16);
-                        const float g1 = __uint_as_float(gw[e / 2] & 0xffff0000u);
-                        v[e] *= __fdividef(1.0f, 1.0f + __expf(-g0));
-                        v[e + 1] *= __fdividef(1.0f, 1.0f + __expf(-g1));
-                    }
-                }
-                uint32_t pk[EPL / 2];
-#pragma unroll
-                for (int e = 0; e < EPL; e += 2)
-                    pk[e / 2] = pack_bf16x2(v[e], v[e + 1]);
-                const size_t off = (tok * p.H + h) * D + lane * EPL;
-                if constexpr (EPL == 4)
-                    *reinterpret_cast<uint2 *>(p.out + off) = make_uint2(pk[0], pk[1]);
-                else
-                    *reinterpret_cast<uint32_t *>(p.out + off) = pk[0];
-            };
-            const int nrows = min(32, rows - quarter * 32);
-            if (gated) {  // fully unrolled: the prefetched gate words are indexed statically
-#pragma unroll
-                for (int i = 0; i < 32; i++)
-                    if (i < nrows)
-                        row_out(i, gpre[i]);
-            } else {
-#pragma unroll 8
-                for (int i = 0; i < nrows; i++)
-                    row_out(i, nullptr);
-            }
         } else if (lane == 0) {
             set_abort(&sm.abort_flag, p.status);
         }
     }
 
     tc::fence_before_sync();
+    __syncthreads();  // the staged rows are complete (unless a wait gave up)
+    if (!aborted(&sm.abort_flag)) {
+        // Lanes across a row, one row per step, this warp's SR rows.
+#pragma unroll
+        for (int i = 0; i < SR; i++) {
+            const int rr = warp * SR + i;
+            if (rr >= rows)
+                break;
+            const float *src = stage + rr * LDS + lane * EPL;
+            float v[EPL];
+            if constexpr (EPL == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src);
+                v[0] = x.x;
+                v[1] = x.y;
+                v[2] = x.z;
+                v[3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(src);
+                v[0] = x.x;
+                v[1] = x.y;
+            }
+            if (split_out) {
+                float *dst = p.part_o + (piece_row0 + rr) * D + lane * EPL;
+                if constexpr (EPL == 4)
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                else
+                    *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+                continue;
+            }
+            if (gated_out) {
+#pragma unroll
+                for (int e = 0; e < EPL; e += 2) {
+                    const float g0 = __uint_as_float(gq[i][e / 2] << 16);
+                    const float g1 = __uint_as_float(gq[i][e / 2] & 0xffff0000u);
+                    v[e] *= __fdividef(1.0f, 1.0f + __expf(-g0));
+                    v[e + 1] *= __fdividef(1.0f, 1.0f + __expf(-g1));
+                }
+            }
+            uint32_t pk[EPL / 2];
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2)
+                pk[e / 2] = pack_bf16x2(v[e], v[e + 1]);
+            const size_t tok = (size_t)(tok0 + r0 + (rr >> pack_shift));
+            const int h = h0 + (rr & (p.pack - 1));
+            const size_t off = (tok * p.H + h) * D + lane * EPL;
+            if constexpr (EPL == 4)
+                *reinterpret_cast<uint2 *>(p.out + off) = make_uint2(pk[0], pk[1]);
+            else
+                *reinterpret_cast<uint32_t *>(p.out + off) = pk[0];
+        }
+    }
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
