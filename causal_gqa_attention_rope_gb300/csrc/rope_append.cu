@@ -421,10 +421,16 @@ __global__ void __launch_bounds__(kAppendThreads) rope_append_kernel(const RopeA
         }
         if (rot) {
             const float fr = f * p.rope_scale;  // the attention factor scales rotated dims only
-            if (qk_norm) {
+            if (qk_norm && zero_centered) {
 #pragma unroll
                 for (int i = 0; i < 8; i++)
                     rotate(xa2[i], xb2[i], cs[i * 8 + k], fr, ya[i], yb[i]);
+            } else if (qk_norm) {
+                // x * w of two bf16 values is exact in fp32 (its low part is 0):
+                // the exact-input rotation gives the same value with fewer terms
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    rotate_exact(xa2[i].hi, xb2[i].hi, cs[i * 8 + k], fr, ya[i], yb[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; i++)
