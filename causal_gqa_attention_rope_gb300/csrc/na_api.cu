@@ -52,6 +52,14 @@ int check_cache(const na_kv_cache *cache, int batch)
     return NA_OK;
 }
 
+// The attention kernels address cache rows (sequence, kv head, slot) through
+// tensor maps whose row coordinate is a signed 32-bit integer.
+int check_cache_rows(const na_kv_cache *cache, int kv_heads)
+{
+    return (long long)cache->batch * kv_heads * cache->capacity > 0x7fffffffLL ? NA_ERR_UNSUPPORTED
+                                                                               : NA_OK;
+}
+
 int sm_count()
 {
     // per device; an unreadable count plans for 152 SMs (the launches then
@@ -321,6 +329,8 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
         return NA_ERR_INVALID_ARG;
     if ((rc = check_cache(cache, batch)) != NA_OK)
         return rc;
+    if ((rc = check_cache_rows(cache, cfg->num_kv_heads)) != NA_OK)
+        return rc;
     if (total_tokens == 0)
         return NA_OK;
     if (!cu_seqlens || !cache_lens || !q_rot || !out || max_new_len <= 0)
@@ -334,8 +344,7 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
     } else if (max_total_len > cache->capacity) {
         return NA_ERR_CAPACITY;
     }
-    if ((long long)cache->batch * cfg->num_kv_heads * cache->capacity >= (1ll << 31) ||
-        (long long)total_tokens * cfg->num_heads * cfg->head_dim >= (1ll << 40))
+    if ((long long)total_tokens * cfg->num_heads * cfg->head_dim >= (1ll << 40))
         return NA_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
     if (!aligned16(q_rot) || !aligned16(out))
         return NA_ERR_INVALID_ARG;
@@ -439,6 +448,8 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     if (batch <= 0 || max_kv_len < 0 || num_splits < 0)
         return NA_ERR_INVALID_ARG;
     if ((rc = check_cache(cache, batch)) != NA_OK)
+        return rc;
+    if ((rc = check_cache_rows(cache, cfg->num_kv_heads)) != NA_OK)
         return rc;
     if (!q_rot || !kv_lens || !out || !aligned16(q_rot) || !aligned16(out))
         return NA_ERR_INVALID_ARG;

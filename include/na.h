@@ -164,6 +164,11 @@ int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_
  *   status        device int32 or NULL: NA_ERR_INVALID_ARG when a new length exceeds
  *                 max_new_len or cu_seqlens[0] != 0, NA_ERR_CAPACITY when a position
  *                 reaches max_total_len or the capacity (those rows are not written).
+ * Errors (before anything is enqueued): NA_ERR_INVALID_ARG for null or misaligned
+ * buffers and negative sizes, NA_ERR_UNSUPPORTED for a ring whose capacity is not
+ * a multiple of 128 or a cache of more than 2^31 - 1 rows (batch x kv heads x
+ * capacity), NA_ERR_CAPACITY when the ring cannot hold a window plus a chunk,
+ * NA_ERR_WORKSPACE for a missing or short workspace.
  */
 int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *cu_seqlens,
                           const int32_t *cache_lens, int32_t total_tokens, int32_t max_new_len,
@@ -203,8 +208,9 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
  * Errors (before anything is enqueued): NA_ERR_INVALID_ARG for null or
  * misaligned buffers, NA_ERR_CAPACITY when max_kv_len (or, with a ring, the
  * window) exceeds the capacity or a stride, NA_ERR_UNSUPPORTED for a ring whose
- * capacity is not a multiple of 64 (keys are read in aligned 64-key tiles),
- * NA_ERR_WORKSPACE for a missing or short workspace.
+ * capacity is not a multiple of 64 (keys are read in aligned 64-key tiles) or a
+ * cache of more than 2^31 - 1 rows (batch x kv heads x capacity: the tensor-map
+ * row coordinate is 32-bit), NA_ERR_WORKSPACE for a missing or short workspace.
  */
 int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
                    const na_kv_cache *cache, const int32_t *kv_lens, int32_t max_kv_len,

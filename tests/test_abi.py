@@ -190,6 +190,19 @@ def test_ring_cache_capacity_rules(lib):
     assert rc == na.NA_ERR_UNSUPPORTED         # decode reads the ring in whole 64-key tiles
 
 
+def test_cache_row_count_limit(lib):
+    """Cache rows (sequences x kv heads x slots) are addressed with 32-bit tensor
+    coordinates: a cache with more rows is refused before any launch."""
+    c = _cfg()
+    huge = na.na_kv_cache(16, 16, 1 << 20, 1 << 12)   # 2^20 x 8 kv heads x 2^12 = 2^35 rows
+    rc = lib.na_attn_prefill_chunk(ctypes.byref(c), 1, 16, 16, 10, 10, 5000, 16,
+                                   ctypes.byref(huge), None, 16, None, 1 << 30, None, None)
+    assert rc == na.NA_ERR_UNSUPPORTED
+    rc = lib.na_attn_decode(ctypes.byref(c), 1, 16, ctypes.byref(huge), 16, 5000, None, 16,
+                            None, 0, 0, 16, 1 << 30, None, None)
+    assert rc == na.NA_ERR_UNSUPPORTED
+
+
 def test_no_fallback_without_the_library(tmp_path, monkeypatch):
     """A missing libna.so raises instead of falling back to any other path."""
     monkeypatch.setattr(na, "_lib", None)
