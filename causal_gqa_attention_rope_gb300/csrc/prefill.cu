@@ -389,6 +389,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- S = Q K^T issue --
         if (lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false, false);
+            // Descriptors of the Q tile and of K stage 0; a 64-wide column block
+            // (BM = BN rows of 128 B) is BLK16 16-byte units, a K stage K_STAGE16.
+            constexpr uint32_t BLK16 = (BM * 128) >> 4;
+            constexpr uint32_t K_STAGE16 = (KB * BN * 128) >> 4;
+            static_assert(BM == BN, "one column-block stride for Q and K");
+            const uint64_t qd0 = tc::desc_kmajor_sw128(smem_addr(sm.q[0]));
+            const uint64_t kd0 = tc::desc_kmajor_sw128(smem_addr(sm.k[0][0]));
             bool ok = mbar_wait_bounded(&sm.q_full, 0);
             bool any = false;
             for (int j = 0; ok && j < n_tiles; j++) {
@@ -400,12 +407,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 tc::fence_after_sync();
                 const uint32_t s_t = tmem + S_COL0 * (sb + 1);
+                const uint64_t kd = kd0 + (uint64_t)(st * K_STAGE16);
 #pragma unroll
-                for (int k = 0; k < D / 16; k++) {
-                    const int kb = k >> 2, kk = k & 3;
-                    const uint64_t a = tc::desc_kmajor_sw128(smem_addr(sm.q[kb]) + kk * 32);
-                    const uint64_t bd = tc::desc_kmajor_sw128(smem_addr(sm.k[st][kb]) + kk * 32);
-                    tc::mma_ss(s_t, a, bd, idesc_s, k > 0);
+                for (int k = 0; k < D / 16; k++) {  // descriptor start addresses advance in 16-byte units
+                    const uint32_t off = (k >> 2) * BLK16 + (k & 3) * 2;
+                    tc::mma_ss(s_t, qd0 + off, kd + off, idesc_s, k > 0);
                 }
                 tc::mma_commit(&sm.s_full[sb]);
                 tc::mma_commit(&sm.k_empty[st]);
@@ -422,6 +428,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // --------------------------------------------------- O += P V issue --
         if (lane == 0) {
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, D, false, true);
+            constexpr uint32_t V_STAGE16 = (KB * BN * 128) >> 4;  // a V stage in 16-byte units
+            const uint64_t vd0 = tc::desc_mnmajor_sw128(smem_addr(sm.v[0][0]), BN * 128);
             bool ok = true, any = false;
             for (int j = 0; ok && j < n_tiles; j++) {
                 const int st = j % STAGES, sb = j % NUM_S;
@@ -432,12 +440,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 tc::fence_after_sync();
                 const uint32_t p_t = tmem + S_COL0 * (sb + 1);
-                const uint32_t vbase = smem_addr(sm.v[st][0]);
+                const uint64_t vd = vd0 + (uint64_t)(st * V_STAGE16);
 #pragma unroll
-                for (int k = 0; k < BN / 16; k++) {
-                    const uint64_t bd = tc::desc_mnmajor_sw128(vbase + k * 16 * 128, BN * 128);
-                    tc::mma_ts(tmem, p_t + k * 8, bd, idesc_o, j > 0 || k > 0);
-                }
+                for (int k = 0; k < BN / 16; k++)  // 16 keys = 16 rows of 128 B per step
+                    tc::mma_ts(tmem, p_t + k * 8, vd + (uint64_t)(k * 128), idesc_o, j > 0 || k > 0);
                 tc::mma_commit(&sm.s_free[sb]);
                 tc::mma_commit(&sm.v_empty[st]);
                 tc::mma_commit(&sm.o_done[sb]);
