@@ -26,9 +26,10 @@
 //              rescaled in tensor memory), exponentiate on the MUFU unit
 //              (measured faster than moving part of the exponentials to a
 //              polynomial on the FMA pipe), write P_j as bf16 over S_j, and
-//              finally normalise and gate O, staging it through the idle K ring
-//              so that each warp stores whole rows (coalesced) instead of one
-//              16-byte piece of 32 different rows per instruction.
+//              finally normalise O and stage it through the idle K ring;
+//   all warps  then gate and store 16 of the staged rows each, a whole row per
+//              instruction (coalesced) instead of one 16-byte piece of 32
+//              different rows; warps 0-3 prefetch their gate rows at the start.
 // With three S buffers the tensor core computes S_{j+1} and S_{j+2} while the
 // softmax works on tile j, and PV_j runs while it prepares P_{j+1}.
 //

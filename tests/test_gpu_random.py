@@ -1,0 +1,107 @@
+"""Seeded random sweeps of the attention calls against the oracle: shapes, head
+groupings, lengths, options (window, soft cap, gate, norms, partial rotary)
+and strides drawn from a fixed generator, so that combinations the hand-picked
+cases do not name are exercised too.  Every case is deterministic.  Inputs are
+unit-scale (std 0.5 or 1), the scale the fixed max-abs bound of 2e-2 is meant
+for: with std 2 outputs reach |6| and one bf16 ulp there is already 0.031 (the
+exact f64 result rounded to bf16 alone is off by 0.015)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from harness import (PROBS_MAX_ABS, Guarded, assert_out_close, assert_probs_close, attn_cfg,
+                     check_cache, gpu_decode, gpu_step, oracle_append, oracle_flags, oracle_rows,
+                     score_scale)
+
+pytestmark = pytest.mark.gpu
+
+HEADS = [(4, 1), (8, 2), (6, 2), (12, 4), (16, 2), (5, 5), (10, 2), (32, 8), (24, 3)]
+
+
+def _random_spec(rng, decode: bool) -> W.Spec:
+    H, KV = HEADS[rng.integers(len(HEADS))]
+    d = int(rng.choice([64, 128]))
+    rd = int(rng.choice([d, d // 2, 16 * int(rng.integers(1, d // 16 + 1))]))
+    yarn = bool(rng.random() < 0.3)
+    rope = W.RopeParams(base=float(rng.choice([1e4, 5e5, 1e6])), yarn=yarn,
+                        factor=4.0 if yarn else 1.0, orig_max_pos=2048 if yarn else 0)
+    return W.Spec(H=H, KV=KV, d=d, rd=rd, rope=rope,
+                  qk_norm=bool(rng.random() < 0.3) and not decode,
+                  v_norm=bool(rng.random() < 0.2) and not decode,
+                  out_gate=bool(rng.random() < 0.4),
+                  softcap=float(rng.choice([0.0, 0.0, 15.0, 50.0])),
+                  window=int(rng.choice([0, 0, 0, int(rng.integers(1, 700))])),
+                  std=float(rng.choice([0.5, 1.0])))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_prefill_steps(oracle, seed):
+    """A few sequences with random histories and new-token counts (some empty)
+    through append + attend; every row compared with the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    spec = _random_spec(rng, decode=False)
+    B = int(rng.integers(1, 5))
+    prior = [int(x) for x in rng.integers(0, 600, B)]
+    new = [int(x) for x in rng.integers(0, 160, B)]
+    if sum(new) == 0:
+        new[0] = 1
+    capacity = (max(p + n for p, n in zip(prior, new)) + 127) // 128 * 128 + 128
+    step = W.make_step(spec, prior, new, capacity, seed=2000 + seed)
+    g = gpu_step(step)
+    assert g.status == 0, f"status {g.status}"
+    ost = oracle_append(oracle, step)
+    check_cache(g.cache_k, g.cache_v, step, ost)
+    rows = list(range(step.total_tokens))
+    ref = oracle_rows(oracle, step, ost, rows)
+    assert_out_close(g.out[rows].to(torch.float64).numpy(), ref,
+                     f"seed {seed}: {spec.H}/{spec.KV} d{spec.d} rd{spec.rd} prior {prior} new {new}")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_decode_steps(oracle, seed):
+    """Random batch, lengths (0 included), options, key splits and probability
+    strides (multiples of 4 or not); outputs and every probability compared,
+    then the Born-rule importance of those probabilities, accumulated onto a
+    random running score."""
+    rng = np.random.default_rng(3000 + seed)
+    spec = _random_spec(rng, decode=True)
+    B = int(rng.integers(1, 9))
+    lens = [int(x) for x in rng.integers(0, 2500, B)]
+    if rng.random() < 0.3:
+        lens[int(rng.integers(B))] = 0
+    capacity = max(max(lens), 1) + int(rng.integers(0, 64))
+    dec = W.make_decode(spec, lens, capacity, seed=4000 + seed)
+    splits = int(rng.choice([0, 0, 1, 3, 7]))
+    stride = max(max(lens), 1) + int(rng.integers(0, 6))
+    out, probs, status = gpu_decode(dec, num_splits=splits, probs_stride=stride)
+    assert status == 0
+    s = dec.spec
+    ref_out, ref_p = oracle.decode(s.H, s.KV, s.d, score_scale(s), oracle_flags(s),
+                                   W.bf16_to_f64(dec.q),
+                                   np.ascontiguousarray(W.bf16_to_f64(dec.cache_k)),
+                                   np.ascontiguousarray(W.bf16_to_f64(dec.cache_v)),
+                                   dec.kv_lens.numpy(), gate=W.bf16_to_f64(dec.gate),
+                                   probs_stride=stride, softcap=s.softcap, window=s.window)
+    what = f"seed {seed}: {s.H}/{s.KV} d{s.d} lens {lens} splits {splits} stride {stride}"
+    assert_out_close(out.double().numpy(), ref_out, what)
+    for b, n in enumerate(lens):
+        assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"{what} probs b{b}")
+        assert bool((probs[b, :, n:] == -7.0).all()), "probs written past kv_len"
+
+    import causal_gqa_attention_rope_gb300 as na
+    init = torch.rand((B, stride), generator=torch.Generator().manual_seed(seed))
+    gi = Guarded((B, stride), torch.float32, "cuda", fill=init.to("cuda"))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    na.na_decode_importance(attn_cfg(s), probs.to("cuda"), dec.kv_lens.to("cuda"),
+                            max(max(lens), 1), gi.t, accumulate=True, status=st)
+    torch.cuda.synchronize()
+    gi.check("importance")
+    assert int(st.item()) == 0
+    ref_imp = oracle.decode_importance(s.H, ref_p, dec.kv_lens.numpy(),
+                                       imp=init.double().numpy(), accumulate=True)
+    got = gi.t.cpu()
+    for b, n in enumerate(lens):
+        err = float(np.max(np.abs(got[b, :n].double().numpy() - ref_imp[b, :n]))) if n else 0.0
+        assert err <= s.H * PROBS_MAX_ABS, f"{what} importance b{b}: {err:.3e}"
+        assert torch.equal(got[b, n:], init[b, n:]), "importance written past kv_len"
