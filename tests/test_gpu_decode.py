@@ -81,8 +81,9 @@ def test_decode_softcap_and_window(oracle, name, spec):
 
 
 def test_decode_ring_cache(oracle):
-    """Ring cache of 448 slots (not a multiple of the key tile) with a window of
-    300: key tiles that cross the end of the ring continue at slot 0."""
+    """Ring cache of 448 slots (seven 64-key tiles; not a multiple of the
+    prefill's 128-key tile) with a window of 300: windows that cross the end of
+    the ring continue at slot 0."""
     import causal_gqa_attention_rope_gb300 as na
     from harness import attn_cfg, ring_from_linear
     spec = W.Spec(H=8, KV=2, d=128, rd=128, window=300)

@@ -12,7 +12,7 @@ import torch
 import workloads as W
 from harness import (PROBS_MAX_ABS, Guarded, assert_out_close, assert_probs_close, attn_cfg,
                      check_cache, gpu_decode, gpu_step, oracle_append, oracle_flags, oracle_rows,
-                     score_scale)
+                     ring_from_linear, score_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -105,3 +105,47 @@ def test_random_decode_steps(oracle, seed):
         err = float(np.max(np.abs(got[b, :n].double().numpy() - ref_imp[b, :n]))) if n else 0.0
         assert err <= s.H * PROBS_MAX_ABS, f"{what} importance b{b}: {err:.3e}"
         assert torch.equal(got[b, n:], init[b, n:]), "importance written past kv_len"
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_decode_ring(oracle, seed):
+    """A ring cache (capacity a multiple of 64 holding at least the window) with
+    random windows and lengths up to three times the ring: windows cross the
+    ring's end at random places."""
+    import causal_gqa_attention_rope_gb300 as na
+    rng = np.random.default_rng(5000 + seed)
+    spec = _random_spec(rng, decode=True)
+    spec.window = int(rng.integers(1, 600))
+    R = (spec.window + int(rng.integers(0, 300)) + 63) // 64 * 64
+    B = int(rng.integers(1, 7))
+    lens = [int(x) for x in rng.integers(0, 3 * R, B)]
+    dec = W.make_decode(spec, lens, max(max(lens), 1), seed=6000 + seed)
+    rk = ring_from_linear(oracle, dec.cache_k, lens, R)
+    rv = ring_from_linear(oracle, dec.cache_v, lens, R)
+    cfg = attn_cfg(spec)
+    cfg.ring_cache = True
+    dev = "cuda"
+    q = dec.q.to(dev)
+    mx = max(max(lens), 1)
+    go = Guarded(q.shape, q.dtype, dev)
+    gp = Guarded((B, spec.H, mx), torch.float32, dev, fill=-7.0)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = na.workspace(na.na_decode_workspace_size(cfg, B, mx), dev)
+    gate = None if dec.gate is None else dec.gate.to(dev)
+    na.na_attn_decode(cfg, q, na.KVCache(rk.to(dev), rv.to(dev)), dec.kv_lens.to(dev), mx, go.t,
+                      probs=gp.t, gate=gate, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    go.check("ring decode out")
+    gp.check("ring decode probs")
+    s = dec.spec
+    ref_out, ref_p = oracle.decode(s.H, s.KV, s.d, score_scale(s), oracle_flags(s, True),
+                                   W.bf16_to_f64(dec.q), np.ascontiguousarray(W.bf16_to_f64(rk)),
+                                   np.ascontiguousarray(W.bf16_to_f64(rv)), dec.kv_lens.numpy(),
+                                   gate=W.bf16_to_f64(dec.gate), probs_stride=mx,
+                                   softcap=s.softcap, window=s.window)
+    what = f"seed {seed}: ring {R} window {s.window} {s.H}/{s.KV} d{s.d} lens {lens}"
+    assert_out_close(go.t.cpu().double().numpy(), ref_out, what)
+    probs = gp.t.cpu()
+    for b, n in enumerate(lens):
+        assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"{what} probs b{b}")
