@@ -136,6 +136,28 @@ def test_prefill_short_chunks(oracle, name):
     _compare_step(oracle, step, what=name)
 
 
+MULTI_WAVE = {
+    # one sequence with at least two whole waves of 128-row units on 152 SMs and
+    # a tail of leftover units (cut into key ranges when few are left)
+    "h40kv8_d64_gate": (W.Spec(H=40, KV=8, d=64, rd=64, out_gate=True), 300, 1024),
+    "h40kv8_d128_softcap": (W.Spec(H=40, KV=8, d=128, rd=64, softcap=30.0), 1000, 1024),
+    "h40kv8_d128_window_gate": (W.Spec(H=40, KV=8, d=128, rd=128, window=700, out_gate=True),
+                                2000, 1024),
+    "h48kv8_d128_tail_whole": (W.Spec(H=48, KV=8, d=128, rd=128), 5000, 1152),
+}
+
+
+@pytest.mark.parametrize("name", list(MULTI_WAVE))
+def test_prefill_multi_wave_single_sequence(oracle, name):
+    """Calls of one sequence with several waves of units and a tail (cut into
+    key ranges or whole); sampled rows of every head against the oracle, the
+    cache bit for bit."""
+    spec, prior, new = MULTI_WAVE[name]
+    capacity = (prior + new + 127) // 128 * 128
+    step = W.make_step(spec, [prior], [new], capacity, seed=131)
+    _compare_step(oracle, step, rows=sample_rows(new, 96, seed=7), what=name)
+
+
 def test_prefill_ring_cache(oracle):
     """Ring cache (slot = position % capacity) with a window: the chunk is
     appended into the ring, every row attends the last `window` keys, and the
