@@ -10,9 +10,9 @@ import pytest
 import torch
 
 import workloads as W
-from harness import (PROBS_MAX_ABS, Guarded, assert_out_close, assert_probs_close, attn_cfg,
-                     check_cache, gpu_decode, gpu_step, oracle_append, oracle_flags, oracle_rows,
-                     ring_from_linear, score_scale)
+from harness import (PROBS_MAX_ABS, Guarded, assert_out_close, assert_probs_close,
+                     assert_within_ulp, attn_cfg, check_cache, gpu_decode, gpu_step, oracle_append,
+                     oracle_flags, oracle_rows, ring_from_linear, rope_cfg, score_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -149,3 +149,47 @@ def test_random_decode_ring(oracle, seed):
     probs = gp.t.cpu()
     for b, n in enumerate(lens):
         assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"{what} probs b{b}")
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_rope_append(oracle, seed):
+    """Any even rotary dim (the register and the staged kernel), both qk-norm
+    styles, V-norm, YaRN factors, explicit attention factors and positions up
+    to 20000: rotated Q and K within 1 ulp, V and untouched slots bit for bit."""
+    rng = np.random.default_rng(7000 + seed)
+    H, KV = HEADS[rng.integers(len(HEADS))]
+    d = int(rng.choice([64, 128]))
+    rd = int(rng.choice([0, d, 2 * int(rng.integers(1, d // 2 + 1))]))
+    yarn = bool(rng.random() < 0.5)
+    rope = W.RopeParams(base=float(rng.choice([1e4, 5e5, 1e6])), yarn=yarn,
+                        factor=float(rng.choice([2.0, 4.0, 8.0])) if yarn else 1.0,
+                        orig_max_pos=int(rng.choice([2048, 4096, 8192])) if yarn else 0,
+                        attn_factor=float(rng.choice([0.0, 0.0, 1.0, 0.75, 1.25])))
+    qk = bool(rng.random() < 0.5)
+    zc = qk and bool(rng.random() < 0.5)
+    spec = W.Spec(H=H, KV=KV, d=d, rd=rd, rope=rope, qk_norm=qk, qk_norm_zero_centered=zc,
+                  v_norm=bool(rng.random() < 0.4), eps=float(rng.choice([1e-6, 1e-5])),
+                  norm_w_mean=0.0 if zc else 1.0)
+    B = int(rng.integers(1, 5))
+    prior = [int(x) for x in rng.integers(0, 20000, B)]
+    new = [int(x) for x in rng.integers(0, 48, B)]
+    if sum(new) == 0:
+        new[0] = 1
+    capacity = max(p + n for p, n in zip(prior, new))
+    # the history itself is never read by the append: sentinel slots stand in
+    step = W.make_step(spec, prior, new, capacity, seed=8000 + seed, history=False)
+    import causal_gqa_attention_rope_gb300 as na
+    dev = lambda x: None if x is None else x.to("cuda").contiguous()
+    cache = na.KVCache(dev(step.cache_k), dev(step.cache_v))
+    gq = Guarded(step.q.shape, step.q.dtype, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    na.na_rope_append_kv(attn_cfg(spec), rope_cfg(spec), dev(step.cu_seqlens),
+                         dev(step.cache_lens), dev(step.q), dev(step.k), dev(step.v), gq.t, cache,
+                         q_norm_w=dev(step.q_norm_w), k_norm_w=dev(step.k_norm_w), status=status,
+                         total_tokens=step.total_tokens)
+    torch.cuda.synchronize()
+    gq.check("q_out")
+    assert int(status.item()) == 0
+    ost = oracle_append(oracle, step)
+    assert_within_ulp(gq.t.cpu(), ost.q_rot, f"seed {seed} rd {rd}: rotated Q")
+    check_cache(cache.k.cpu(), cache.v.cpu(), step, ost)
