@@ -33,6 +33,19 @@ def _check(oracle, dec, num_splits=0, with_probs=True):
             assert bool((probs[b, :, n:] == -7.0).all()), "probs written past kv_len"
 
 
+def _assert_probs_relative(gpu, ref, what):
+    """Each probability within 1e-4 of its own value (plus 1e-9).  Over
+    thousands of keys the probabilities are ~1e-4..1e-5 and the fixed max-abs
+    bound says little; with unit-scale inputs a score is off by ~1e-6, which
+    moves its probability by ~1e-6 of itself (1.5e-6 the worst measured at
+    131072 keys), and a missing, doubled or misplaced key moves it by far
+    more."""
+    g, r = gpu.double().numpy(), ref
+    bad = np.abs(g - r) > 1e-4 * r + 1e-9
+    assert not bad.any(), (f"{what}: {int(bad.sum())} probabilities beyond 1e-4 relative; "
+                           f"worst {float(np.max(np.abs(g - r) / (r + 1e-9))):.3e}")
+
+
 SHAPES = {
     "h32kv8d128": W.Spec(H=32, KV=8, d=128, rd=128),
     "h4kv1d128_group4": W.Spec(H=4, KV=1, d=128, rd=128),
@@ -64,6 +77,24 @@ def test_decode_balanced_slices_skip_empty_sequences(oracle, splits):
     lens = [0] * 37 + [3000] + [1, 0] * 15 + [0, 257, 0]
     dec = W.make_decode(W.Spec(H=8, KV=2, d=128, rd=128), lens, 3072, seed=93)
     _check(oracle, dec, num_splits=splits)
+
+
+@pytest.mark.parametrize("name,spec", [
+    ("plain", W.Spec(H=4, KV=1, d=128, rd=128)),
+    ("window4096_gate", W.Spec(H=8, KV=1, d=64, rd=64, window=4096, out_gate=True)),
+])
+def test_decode_long_context(oracle, name, spec):
+    """A 131072-key sequence beside a 50001-key one and a 1-key one: the long
+    ones are cut into many equal key slices (pieces of one stream spread over
+    most of the grid) and merged; with a window only its last 4096 keys count
+    and every probability before them is 0."""
+    dec = W.make_decode(spec, [131072, 50001, 1], 131072, seed=107)
+    _check(oracle, dec)
+    out, probs, status = gpu_decode(dec, with_probs=True)
+    assert status == 0
+    _, ref_p = _oracle_decode(oracle, dec, stride=probs.shape[-1])
+    for b, n in enumerate(dec.kv_lens.tolist()):
+        _assert_probs_relative(probs[b, :, :n], ref_p[b, :, :n], f"{name} b{b}")
 
 
 @pytest.mark.parametrize("name,spec", [
@@ -157,6 +188,7 @@ def test_full_decode_b64_h32kv8_kv512to8192(oracle):
         b, h = divmod(r, H)
         assert_out_close(out[b, h].double().numpy(), ref_out[b, h], f"row {r}")
         assert_probs_close(probs[b, h, :lens[b]].numpy(), ref_p[b, h, :lens[b]], f"probs {r}")
+        _assert_probs_relative(probs[b, h, :lens[b]], ref_p[b, h, :lens[b]], f"probs {r}")
 
 
 # ----------------------------------------------------- Born-rule importance --
