@@ -24,8 +24,10 @@ over the cache the step fills), so it is measured in the same launch
 configuration as the step and never exceeds it.  The end-to-end figure (`e2e`)
 runs the headline step through the public API with host buffers: the prompt
 is copied in from pinned host memory and the output copied back inside the
-timed region.  `--impl reference` times the f64 CPU oracle on a bounded sample
-of the headline workload instead.
+timed region.  Chunked prompts are also timed eager (`eager`: the same calls
+launched from Python every step, device buffers, same flushes).
+`--impl reference` times the f64 CPU oracle on a bounded sample of the
+headline workload instead.
 """
 from __future__ import annotations
 
@@ -230,6 +232,24 @@ def time_graph(g, steps, warmup, flush):
     return ts
 
 
+def time_eager(run, steps, warmup, flush):
+    """Milliseconds of `steps` eager runs (the calls launched from Python each
+    time), each after an L2 flush (not timed)."""
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return ts
+
+
 def kernel_fingerprint(*names) -> str:
     h = hashlib.sha256()
     for n in names:
@@ -360,14 +380,19 @@ def bench_chunked(wl: W.PrefillWorkload, steps: int, warmup: int, peaks, flush,
     g_step, g_attn = capture(run_step), capture(run_attn)
     step_ms = time_graph(g_step, steps, warmup, flush)
     attn_ms = time_graph(g_attn, steps, warmup, flush)
+    eager_ms = time_eager(run_step, steps, warmup, flush)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     launches = len(chunks) + attn_launches
-    st, at = spread(step_ms), spread(attn_ms)
+    st, at, et = spread(step_ms), spread(attn_ms), spread(eager_ms)
     res = {"workload": wl.name, "metric": "prefill attn TFLOP/s", "unit": "TFLOP/s",
            "value": flops_total / (st["median"] * 1e-3) / 1e12, "ms_per_step": st["median"],
            "ms_spread": st, "flops_per_step": flops_total, "launches_per_step": launches,
            "attn_calls_ms": at,
+           "eager": {"value": flops_total / (et["median"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                     "ms_per_step": et["median"], "ms_spread": et,
+                     "launch": "the same calls launched from Python every step (no graph), "
+                               "device buffers"},
            "roofline": tensor_roofline(flops_total, at["median"], peaks,
                                        "na_attn_prefill_chunk (its calls of the step, graph-"
                                        "replayed)", traffic_from_profiles("prefill.cu", wl.name))}
@@ -823,6 +848,9 @@ def main(argv=None):
     line = dict(base_line(args, wl), value=value, ms_per_step=ms, ms_spread=r["ms_spread"])
     line["e2e"] = dict(r["e2e"], value=r["flops_per_step"] * world / (e2e_ms * 1e-3) / 1e12,
                        ms_per_step=e2e_ms)
+    eager_ms = max_over_ranks(r["eager"]["ms_per_step"], world)
+    line["eager"] = dict(r["eager"], value=r["flops_per_step"] * world / (eager_ms * 1e-3) / 1e12,
+                         ms_per_step=eager_ms)
     line["gpu_launches"] = r["launches_per_step"] * args.steps
     line["roofline"] = r["roofline"]
     line["attn_calls_ms"] = r["attn_calls_ms"]
