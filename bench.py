@@ -574,39 +574,47 @@ def bench_decode(wl: W.DecodeWorkload, steps, warmup, peaks, flush):
 
 def bench_pair_verify(steps, warmup, peaks, flush):
     """Speculative pair verify: every sequence of the decode workload checks two
-    drafted tokens (a 2-token chunk after kv_len - 2 cached ones).  HBM-bound:
-    the K/V of each (sequence, kv head) is streamed once for both tokens and
-    all query heads of the group (GQA-packed tiles)."""
+    drafted tokens (a 2-token chunk after kv_len - 2 cached ones).  A step is
+    the append of the drafted tokens, then the attention call, which is
+    HBM-bound: the K/V of each (sequence, kv head) is streamed once for both
+    tokens and all query heads of the group (GQA-packed tiles)."""
     import causal_gqa_attention_rope_gb300 as na
     wl = W.C3
     s = wl.spec
-    gen = torch.Generator().manual_seed(3)
-    lens = W.draw_lengths(gen, wl.batch, *wl.kv_range)
-    step = W.make_step(s, [n - 2 for n in lens], [2] * wl.batch, wl.capacity, seed=5)
+    step = W.make_pair_verify_step()
+    lens = [int(x) + 2 for x in step.cache_lens.tolist()]
     dev = "cuda"
-    cfg = attn_cfg(s)
+    cfg, rope = attn_cfg(s), rope_cfg(s)
     cu, cl = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
-    q = step.q.to(dev)
-    out = torch.empty_like(q)
+    q, k, v = step.q.to(dev), step.k.to(dev), step.v.to(dev)
+    q_out, out = torch.empty_like(q), torch.empty_like(q)
     cache = na.KVCache(step.cache_k.to(dev), step.cache_v.to(dev))
     T, mt = int(step.cu_seqlens[-1]), max(lens)
-    ws = na.workspace(na.na_prefill_workspace_size(cfg, wl.batch, T, 2, mt), dev)
+    wsb = na.na_prefill_workspace_size(cfg, wl.batch, T, 2, mt)
+    ws = na.workspace(wsb, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    def attend():
+        na.na_attn_prefill_chunk(cfg, cu, cl, 2, mt, q_out, cache, out, workspace=ws,
+                                 status=status)
+
     def run():
-        na.na_attn_prefill_chunk(cfg, cu, cl, 2, mt, q, cache, out, workspace=ws, status=status)
+        na.na_rope_append_kv(cfg, rope, cu, cl, q, k, v, q_out, cache, status=status)
+        attend()
 
     for _ in range(warmup):
         run()
     torch.cuda.synchronize()
     st = spread(time_graph(capture(run), steps, warmup, flush))
+    kt = spread(time_graph(capture(attend), steps, warmup, flush))
     assert int(status.item()) == 0
     kv_bytes = sum(lens) * s.KV * s.d * 2 * 2
     name = "pair_verify_b64_h32kv8d128_kv512to8192"
     return {"workload": name, "metric": "pair verify KV GB/s", "unit": "GB/s",
             "value": kv_bytes / (st["median"] * 1e-3) / 1e9, "ms_per_step": st["median"],
-            "ms_spread": st, "bytes_per_step": kv_bytes,
-            "roofline": hbm_roofline(kv_bytes, st["median"], peaks,
+            "ms_spread": st, "attn_call_ms": kt, "bytes_per_step": kv_bytes,
+            "launches_per_step": 2 + (1 if wsb > 0 else 0),
+            "roofline": hbm_roofline(kv_bytes, kt["median"], peaks,
                                      "na_attn_prefill_chunk (2-token chunks, GQA-packed tiles)",
                                      traffic_from_profiles("prefill.cu", name))}
 

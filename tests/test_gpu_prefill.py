@@ -158,6 +158,43 @@ def test_prefill_multi_wave_single_sequence(oracle, name):
     _compare_step(oracle, step, rows=sample_rows(new, 96, seed=7), what=name)
 
 
+def _sequences_of(step: W.StepInputs, idx):
+    """The sub-step holding only sequences `idx` of a packed step (their tokens,
+    bounds and caches), and the packed rows those tokens had."""
+    cu = step.cu_seqlens.tolist()
+    rows = [t for b in idx for t in range(cu[b], cu[b + 1])]
+    new = [cu[b + 1] - cu[b] for b in idx]
+    pick = lambda x: None if x is None else x[rows].contiguous()
+    sub = W.StepInputs(spec=step.spec,
+                       cu_seqlens=torch.tensor(np.concatenate([[0], np.cumsum(new)]),
+                                               dtype=torch.int32),
+                       cache_lens=step.cache_lens[idx].clone(), q=pick(step.q), k=pick(step.k),
+                       v=pick(step.v), gate=pick(step.gate), q_norm_w=step.q_norm_w,
+                       k_norm_w=step.k_norm_w, cache_k=step.cache_k[idx].contiguous(),
+                       cache_v=step.cache_v[idx].contiguous())
+    return sub, rows
+
+
+def test_full_pair_verify_b64(oracle):
+    """The pair-verify workload at full size, as the benchmark runs it: 64
+    sequences each appending 2 drafted tokens after 510..8190 cached ones, then
+    one attention call over all of them (more than 32 sequences: the slots are
+    not ranked by length).  Eight sequences, the longest and the shortest among
+    them, are checked against the oracle: every row of every head and their
+    caches bit for bit."""
+    step = W.make_pair_verify_step()
+    g = gpu_step(step)
+    assert g.status == 0, f"status {g.status}"
+    lens = step.cache_lens.tolist()
+    idx = sorted({int(np.argmax(lens)), int(np.argmin(lens))} |
+                 set(sample_rows(len(lens), 6, seed=17)))
+    sub, rows = _sequences_of(step, idx)
+    ost = oracle_append(oracle, sub)
+    check_cache(g.cache_k[idx], g.cache_v[idx], sub, ost)
+    ref = oracle_rows(oracle, sub, ost, list(range(sub.total_tokens)))
+    assert_out_close(g.out[rows].to(torch.float64).numpy(), ref, f"pair verify sequences {idx}")
+
+
 def test_prefill_ring_cache(oracle):
     """Ring cache (slot = position % capacity) with a window: the chunk is
     appended into the ring, every row attends the last `window` keys, and the

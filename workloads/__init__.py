@@ -291,6 +291,15 @@ def make_decode_workload(w: DecodeWorkload, seed: int = 0) -> DecodeInputs:
     return make_decode(w.spec, lens, w.capacity, seed, gen=gen)
 
 
+def make_pair_verify_step(seed: int = 5) -> StepInputs:
+    """Speculative pair verify over the decode workload: each of its 64
+    sequences (lengths drawn as for the decode, kv_len ~ U{512..8192}) holds
+    kv_len - 2 cached tokens and brings 2 drafted ones."""
+    gen = torch.Generator().manual_seed(3)
+    lens = draw_lengths(gen, C3.batch, *C3.kv_range)
+    return make_step(C3.spec, [n - 2 for n in lens], [2] * C3.batch, C3.capacity, seed=seed)
+
+
 def bf16_to_f64(t: Optional[torch.Tensor]):
     """Exact widening of bf16 data for the oracle (no arithmetic)."""
     if t is None:
