@@ -193,3 +193,64 @@ def test_random_rope_append(oracle, seed):
     ost = oracle_append(oracle, step)
     assert_within_ulp(gq.t.cpu(), ost.q_rot, f"seed {seed} rd {rd}: rotated Q")
     check_cache(cache.k.cpu(), cache.v.cpu(), step, ost)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_prefill_ring(oracle, seed):
+    """Append + attend on a ring cache (capacity a multiple of 128 holding at
+    least window + chunk - 1 positions) with random windows, histories up to
+    three times the ring and chunks of up to 160 tokens, so both the appended
+    slots and the windows wrap around the ring's end at random places; every
+    row against the oracle attending the same ring, the ring slot by slot."""
+    import causal_gqa_attention_rope_gb300 as na
+    rng = np.random.default_rng(9000 + seed)
+    spec = _random_spec(rng, decode=False)
+    spec.window = int(rng.integers(1, 600))
+    B = int(rng.integers(1, 4))
+    new = [int(x) for x in rng.integers(0, 161, B)]
+    if sum(new) == 0:
+        new[0] = 1
+    R = (spec.window + max(new) - 1 + int(rng.integers(0, 200)) + 127) // 128 * 128
+    prior = [int(x) for x in rng.integers(0, 3 * R, B)]
+    step = W.make_step(spec, prior, new, max(p + n for p, n in zip(prior, new)), seed=9100 + seed)
+    ck = ring_from_linear(oracle, step.cache_k, prior, R)
+    cv = ring_from_linear(oracle, step.cache_v, prior, R)
+    ring_step = W.StepInputs(**{**step.__dict__, "cache_k": ck, "cache_v": cv})
+    cfg = attn_cfg(spec)
+    cfg.ring_cache = True
+    dev = "cuda"
+    dv = lambda x: None if x is None else x.to(dev).contiguous()
+    cache = na.KVCache(ck.clone().to(dev), cv.clone().to(dev))
+    q = dv(step.q)
+    gq, go = Guarded(q.shape, q.dtype, dev), Guarded(q.shape, q.dtype, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cu, lens = dv(step.cu_seqlens), dv(step.cache_lens)
+    T = step.total_tokens
+    max_new, max_tot = max(new), max(p + n for p, n in zip(prior, new))
+    na.na_rope_append_kv(cfg, rope_cfg(spec), cu, lens, q, dv(step.k), dv(step.v), gq.t, cache,
+                         q_norm_w=dv(step.q_norm_w), k_norm_w=dv(step.k_norm_w), status=status)
+    ws = na.workspace(na.na_prefill_workspace_size(cfg, B, T, max_new, max_tot), dev)
+    na.na_attn_prefill_chunk(cfg, cu, lens, max_new, max_tot, gq.t, cache, go.t, gate=dv(step.gate),
+                             workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    gq.check("ring q_out")
+    go.check("ring out")
+    what = (f"seed {seed}: ring {R} window {spec.window} {spec.H}/{spec.KV} d{spec.d} "
+            f"rd{spec.rd} prior {prior} new {new}")
+    ost = oracle_append(oracle, ring_step, ring=True)
+    assert_within_ulp(gq.t.cpu(), ost.q_rot, f"{what}: rotated Q")
+    ref = oracle_rows(oracle, ring_step, ost, list(range(T)), ring=True)
+    assert_out_close(go.t.cpu().double().numpy(), ref, what)
+    gk, gv = cache.k.cpu(), cache.v.cpu()
+    for b in range(B):
+        written = sorted({oracle.ring_slot(p, R) for p in range(prior[b], prior[b] + new[b])})
+        kept = sorted(set(range(R)) - set(written))
+        if written:
+            assert_within_ulp(gk[b][:, written], ost.cache_k[b][:, written], f"{what}: ring K b{b}")
+            if spec.v_norm:
+                assert_within_ulp(gv[b][:, written], ost.cache_v[b][:, written], f"{what}: ring V b{b}")
+            else:
+                assert np.array_equal(gv[b][:, written].double().numpy(), ost.cache_v[b][:, written])
+        assert torch.equal(gk[b][:, kept].view(torch.int16), ck[b][:, kept].view(torch.int16))
+        assert torch.equal(gv[b][:, kept].view(torch.int16), cv[b][:, kept].view(torch.int16))
