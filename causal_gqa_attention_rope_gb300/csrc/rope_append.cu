@@ -27,9 +27,11 @@
 //   - rope_append_staged_kernel (any even rotary_dim): the rows are staged in
 //     shared memory and every thread works on independent (row, pair) slots.
 //
-// Precision.  The stored bf16 value is the correctly rounded result of the
-// exact rotation, or one ulp off it only where the rotated value is below
-// ~2^-35 of its inputs:
+// Precision.  Before its final rounding to bf16 a rotated value differs from
+// the exact rotation by at most ~2^-23 of its own magnitude (plus ~2^-43 of
+// its inputs), so the stored bf16 is the correctly rounded value unless the
+// exact one lies that close to a bf16 rounding boundary; then it may be the
+// neighbour, one ulp off (measured: about 7 in a million rotated values):
 //   - The angle is taken in turns: pos * inv_freq / (2 pi) is formed exactly
 //     modulo 1 in 64-bit fixed point (inv_freq / (2 pi) is passed as a 96-bit
 //     fixed-point fraction, from a double-double division on the host; the
@@ -39,11 +41,14 @@
 //     in fp32 pairs (hi + lo, fmaf residuals for the leading products), and the
 //     two are combined with the angle-sum formulas.  Absolute error of cos and
 //     sin below 2^-43 (the rounding of the ~3e-7 low parts).
-//   - The rotation is evaluated with error-free fp32 products (fmaf residuals)
-//     and an error-free sum; the norm weight enters as the exact product x * w
-//     of two bf16 values (for the zero-centred style, x + x * w is kept as an
-//     fp32 hi + lo pair); the row factors (1 / rms, and the attention factor on
-//     the rotated dims) are applied last as one relative rounding.
+//   - The rotation keeps every rounding relative to its own result: one of the
+//     two leading products is split exactly (its error recovered by an fmaf),
+//     the other enters an fmaf unrounded (inputs carried as fp32 pairs use
+//     error-free products and sums instead); the norm weight enters as the
+//     exact product x * w of two bf16 values (for the zero-centred style,
+//     x + x * w is kept as an fp32 hi + lo pair); the row factors (1 / rms,
+//     and the attention factor on the rotated dims) are applied last as one
+//     relative rounding.
 #include "na_internal.cuh"
 
 namespace {
@@ -221,27 +226,28 @@ __device__ __forceinline__ void rotate(F2 a0, F2 a1, float4 c, float fr, float &
     y1 = fmaf(r1.hi, fr, r1.lo * fr);
 }
 
-// The same for exact inputs (no low parts): a0 cos - a1 sin with both leading
-// products exact (fmaf residuals), their sum error-free, the low parts of cos
-// and sin entering once.
+// The same for exact inputs (no low parts).  Of the two leading products one
+// is split exactly -- t = a1 sin_hi rounded, e its error from an fma -- and
+// the other enters an fma unrounded, so h = a0 cos_hi - t carries a single
+// rounding relative to itself; e and the low parts of cos and sin are added
+// once.  Before the final rounding to bf16 the result is within ~2^-23 of
+// itself (plus ~2^-48 of the inputs).
 __device__ __forceinline__ void rotate_exact(float a0, float a1, float4 c, float fr, float &y0,
                                              float &y1)
 {
     {
-        const float p0 = a0 * c.x, e0 = fmaf(a0, c.x, -p0);
-        const float p1 = -a1 * c.z, e1 = fmaf(-a1, c.z, -p1);
-        const float s = p0 + p1, bb = s - p0;
-        const float t = (p0 - (s - bb)) + (p1 - bb);
-        const float lo = t + (e0 + e1) + fmaf(a0, c.y, -a1 * c.w);
-        y0 = fmaf(s, fr, lo * fr);
+        const float t = a1 * c.z;
+        const float e = fmaf(a1, c.z, -t);
+        const float h = fmaf(a0, c.x, -t);
+        const float lo = fmaf(a0, c.y, -a1 * c.w) - e;
+        y0 = fmaf(h, fr, lo * fr);
     }
     {
-        const float p0 = a0 * c.z, e0 = fmaf(a0, c.z, -p0);
-        const float p1 = a1 * c.x, e1 = fmaf(a1, c.x, -p1);
-        const float s = p0 + p1, bb = s - p0;
-        const float t = (p0 - (s - bb)) + (p1 - bb);
-        const float lo = t + (e0 + e1) + fmaf(a0, c.w, a1 * c.y);
-        y1 = fmaf(s, fr, lo * fr);
+        const float t = a1 * c.x;
+        const float e = fmaf(a1, c.x, -t);
+        const float h = fmaf(a0, c.z, t);
+        const float lo = fmaf(a0, c.w, a1 * c.y) + e;
+        y1 = fmaf(h, fr, lo * fr);
     }
 }
 
