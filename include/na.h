@@ -115,6 +115,10 @@ typedef struct na_kv_cache {
  * (slot pos % capacity instead of pos with NA_RING_CACHE).
  * RoPE turns pairs (x[i], x[i + rd/2]), i < rd/2, by pos * inv_freq[i] and
  * multiplies both outputs by the attention factor.
+ * Accuracy: each stored rotated or normed value is within one bf16 ulp of the
+ * exact result: the correctly rounded value unless the exact one lies within
+ * ~2^-23 (relative) of a bf16 rounding boundary (about 7 values in a million);
+ * V without V-norm is stored bit for bit.
  *
  *   cfg, rope     HOST structs.
  *   batch         number of sequences (>= 1, <= cache->batch).
