@@ -153,6 +153,10 @@ int na_rope_append_kv(const na_attn_cfg *cfg, const na_rope_params *rope, int32_
  * cfg->softcap > 0 each scaled score is capped before the softmax.  Chunks of a
  * few tokens per sequence (the drafted tokens of a speculative verify) are
  * valid chunks: each attends the cache plus its own earlier tokens.
+ * Arithmetic: Q.K and P.V on bf16 tensor cores with fp32 accumulation, the
+ * softmax in fp32 with P rounded to bf16 for the P.V product; with unit-scale
+ * inputs the output is within 2e-2 (max-abs) and 5e-3 (relative L2) of the
+ * exact result.
  *
  *   cu_seqlens    int32 [batch + 1], non-decreasing, cu_seqlens[0] == 0.
  *   cache_lens    int32 [batch]: prior lengths (the same values given to na_rope_append_kv).
@@ -186,6 +190,9 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
  *  eviction scoring), fns qwen_attention_core and attend_all_heads: the current
  *  token is appended first, then each group's K/V are streamed once for all its
  *  query heads.]
+ * Arithmetic: bf16 MMAs with fp32 accumulation, softmax and probabilities in
+ * fp32; with unit-scale inputs the output is within 2e-2 (max-abs) of the exact
+ * result and each probability within 1e-4 (measured ~1.5e-6 of its own value).
  *
  *   q_rot      bf16 [batch][H][d], already rotated (one query per sequence).
  *   kv_lens    int32 [batch]: keys to attend, current token included (0 gives a zero
