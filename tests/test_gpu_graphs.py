@@ -1,0 +1,140 @@
+"""The calls under CUDA graph capture, as a serving loop uses them: captured
+once, then replayed with new values in the same buffers -- new queries, new
+lengths, new positions within the bounds given at capture.  Nothing but
+pointers, host bounds and the plan derived from them may be baked into the
+graph: every replay must equal the eager calls on the same inputs bit for bit
+(every kernel here is deterministic: fixed summation orders, no atomics)."""
+import pytest
+import torch
+
+import workloads as W
+from harness import attn_cfg, rope_cfg
+
+pytestmark = pytest.mark.gpu
+
+
+def _capture(fn):
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
+
+
+def test_decode_and_importance_replayed_with_new_lengths():
+    """Decode (with probabilities) + accumulated importance captured with
+    max_kv_len 3000; replayed after the lengths grow, shrink and hit zero and
+    the queries change: each replay equals the eager calls."""
+    import causal_gqa_attention_rope_gb300 as na
+    spec = W.Spec(H=16, KV=4, d=128, rd=128, out_gate=True)
+    B, cap, mx = 5, 3072, 3000
+    dec = W.make_decode(spec, [3000] * B, cap, seed=201)
+    dev = "cuda"
+    cfg = attn_cfg(spec)
+    cache = na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev))
+    q = torch.empty_like(dec.q, device=dev)
+    gate = dec.gate.to(dev)
+    kv = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    probs = torch.full((B, spec.H, mx), -7.0, device=dev)
+    imp = torch.zeros(B, mx, device=dev)
+    ws = na.workspace(na.na_decode_workspace_size(cfg, B, mx), dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        na.na_attn_decode(cfg, q, cache, kv, mx, out, probs=probs, gate=gate, workspace=ws,
+                          status=st)
+        na.na_decode_importance(cfg, probs, kv, mx, imp, accumulate=True, status=st)
+
+    gen = torch.Generator().manual_seed(7)
+    q.copy_(dec.q)
+    kv.copy_(torch.tensor([3000, 1, 64, 700, 0], dtype=torch.int32))
+    g = _capture(step)
+    for lens in ([3000, 1, 64, 700, 0], [2999, 2, 65, 701, 1], [5, 0, 1500, 3000, 63]):
+        newq = torch.randn(dec.q.shape, generator=gen).to(torch.bfloat16)
+        results = []
+        for run in ("graph", "eager"):
+            q.copy_(newq)
+            kv.copy_(torch.tensor(lens, dtype=torch.int32))
+            probs.fill_(-7.0)
+            imp.fill_(0.25)
+            if run == "graph":
+                g.replay()
+            else:
+                step()
+            torch.cuda.synchronize()
+            results.append((out.clone(), probs.clone(), imp.clone()))
+        assert int(st.item()) == 0
+        assert bool(torch.isfinite(results[0][0].float()).all())
+        for a, b, what in zip(results[0], results[1], ("out", "probs", "importance")):
+            assert torch.equal(_bits(a), _bits(b)), f"{what} differs from eager with lengths {lens}"
+
+
+def test_chunked_prefill_replayed_at_new_positions():
+    """Append + attend of a 96-token chunk of two sequences (the attention's
+    cut units and merge pass included) captured with max_total_len 1024;
+    replayed with other prior lengths and new token values: outputs, rotated
+    queries and the cache equal the eager calls."""
+    import causal_gqa_attention_rope_gb300 as na
+    spec = W.Spec(H=8, KV=2, d=128, rd=128, qk_norm=True, out_gate=True,
+                  rope=W.RopeParams(base=5e5))
+    new = [64, 32]
+    cap, max_total = 1024, 1024
+    base = W.make_step(spec, [900, 700], new, cap, seed=203)
+    dev = "cuda"
+    cfg, rope = attn_cfg(spec), rope_cfg(spec)
+    T = base.total_tokens
+    cu = base.cu_seqlens.to(dev)
+    lens = torch.empty(2, dtype=torch.int32, device=dev)
+    q, k, v = (torch.empty_like(x, device=dev) for x in (base.q, base.k, base.v))
+    gate = base.gate.to(dev)
+    qw, kw = base.q_norm_w.to(dev), base.k_norm_w.to(dev)
+    # every slot holds a real key and value, so any prior length attends data
+    cg = torch.Generator().manual_seed(205)
+    ck = torch.randn(base.cache_k.shape, generator=cg).to(torch.bfloat16).to(dev)
+    cv = torch.randn(base.cache_v.shape, generator=cg).to(torch.bfloat16).to(dev)
+    cache = na.KVCache(ck.clone(), cv.clone())
+    q_out, out = torch.empty_like(q), torch.empty_like(q)
+    ws = na.workspace(na.na_prefill_workspace_size(cfg, 2, T, max(new), max_total), dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        na.na_rope_append_kv(cfg, rope, cu, lens, q, k, v, q_out, cache, q_norm_w=qw,
+                             k_norm_w=kw, status=st)
+        na.na_attn_prefill_chunk(cfg, cu, lens, max(new), max_total, q_out, cache, out,
+                                 gate=gate, workspace=ws, status=st)
+
+    gen = torch.Generator().manual_seed(9)
+    for x, y in ((q, base.q), (k, base.k), (v, base.v)):
+        x.copy_(y)
+    lens.copy_(torch.tensor([900, 700], dtype=torch.int32))
+    g = _capture(step)
+    for prior in ([900, 700], [960, 0], [100, 992], [0, 5]):
+        vals = [torch.randn(x.shape, generator=gen).to(torch.bfloat16) for x in (base.q, base.k, base.v)]
+        results = []
+        for run in ("graph", "eager"):
+            for x, y in zip((q, k, v), vals):
+                x.copy_(y)
+            lens.copy_(torch.tensor(prior, dtype=torch.int32))
+            cache.k.copy_(ck)
+            cache.v.copy_(cv)
+            if run == "graph":
+                g.replay()
+            else:
+                step()
+            torch.cuda.synchronize()
+            results.append((out.clone(), q_out.clone(), cache.k.clone(), cache.v.clone()))
+        assert int(st.item()) == 0
+        assert bool(torch.isfinite(results[0][0].float()).all())
+        for a, b, what in zip(results[0], results[1], ("out", "q_out", "cache K", "cache V")):
+            assert torch.equal(_bits(a), _bits(b)), f"{what} differs from eager with priors {prior}"
