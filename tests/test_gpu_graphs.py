@@ -1,9 +1,10 @@
-"""The calls under CUDA graph capture, as a serving loop uses them: captured
-once, then replayed with new values in the same buffers -- new queries, new
-lengths, new positions within the bounds given at capture.  Nothing but
+"""The calls as a serving loop uses them: under CUDA graph capture -- captured
+once, then replayed with new values in the same buffers (new queries, new
+lengths, new positions within the bounds given at capture), where nothing but
 pointers, host bounds and the plan derived from them may be baked into the
-graph: every replay must equal the eager calls on the same inputs bit for bit
-(every kernel here is deterministic: fixed summation orders, no atomics)."""
+graph -- and on several streams at once.  Every run must equal the eager,
+one-at-a-time calls on the same inputs bit for bit (every kernel here is
+deterministic: fixed summation orders, no atomics)."""
 import pytest
 import torch
 
@@ -138,3 +139,67 @@ def test_chunked_prefill_replayed_at_new_positions():
         assert bool(torch.isfinite(results[0][0].float()).all())
         for a, b, what in zip(results[0], results[1], ("out", "q_out", "cache K", "cache V")):
             assert torch.equal(_bits(a), _bits(b)), f"{what} differs from eager with priors {prior}"
+
+
+def test_calls_on_two_streams_at_once():
+    """A decode on one stream and an append + attend on another, launched
+    without waiting for each other (each with its own workspace and status):
+    both equal the same calls run one after the other -- no device state is
+    shared between calls."""
+    import causal_gqa_attention_rope_gb300 as na
+    dev = "cuda"
+    # decode
+    dspec = W.Spec(H=32, KV=8, d=128, rd=128)
+    dec = W.make_decode(dspec, [4000, 17, 2500, 900], 4096, seed=211)
+    dcfg = attn_cfg(dspec)
+    dq, dkv = dec.q.to(dev), dec.kv_lens.to(dev)
+    dcache = na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev))
+    dout = torch.empty_like(dq)
+    dprobs = torch.zeros(4, dspec.H, 4000, device=dev)
+    dws = na.workspace(na.na_decode_workspace_size(dcfg, 4, 4000), dev)
+    dst = torch.zeros(1, dtype=torch.int32, device=dev)
+    # prefill
+    pspec = W.Spec(H=8, KV=2, d=64, rd=64, out_gate=True)
+    step = W.make_step(pspec, [600, 40], [150, 70], 1024, seed=213)
+    pcfg, prope = attn_cfg(pspec), rope_cfg(pspec)
+    cu, lens = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
+    q, k, v, gate = (x.to(dev) for x in (step.q, step.k, step.v, step.gate))
+    ck0, cv0 = step.cache_k.to(dev), step.cache_v.to(dev)
+    pcache = na.KVCache(ck0.clone(), cv0.clone())
+    q_out, pout = torch.empty_like(q), torch.empty_like(q)
+    T = step.total_tokens
+    pws = na.workspace(na.na_prefill_workspace_size(pcfg, 2, T, 150, 750), dev)
+    pst = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def decode():
+        na.na_attn_decode(dcfg, dq, dcache, dkv, 4000, dout, probs=dprobs, workspace=dws,
+                          status=dst)
+
+    def prefill():
+        na.na_rope_append_kv(pcfg, prope, cu, lens, q, k, v, q_out, pcache, status=pst)
+        na.na_attn_prefill_chunk(pcfg, cu, lens, 150, 750, q_out, pcache, pout, gate=gate,
+                                 workspace=pws, status=pst)
+
+    def snapshot():
+        torch.cuda.synchronize()
+        return [t.clone() for t in (dout, dprobs, pout, q_out, pcache.k, pcache.v)]
+
+    decode()
+    prefill()
+    ref = snapshot()
+    for _ in range(3):
+        dout.zero_()
+        dprobs.zero_()
+        pout.zero_()
+        pcache.k.copy_(ck0)
+        pcache.v.copy_(cv0)
+        torch.cuda.synchronize()
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        with torch.cuda.stream(s1):
+            decode()
+        with torch.cuda.stream(s2):
+            prefill()
+        got = snapshot()
+        assert int(dst.item()) == 0 and int(pst.item()) == 0
+        for a, b in zip(got, ref):
+            assert torch.equal(_bits(a), _bits(b))
