@@ -3,7 +3,9 @@ or 128 query heads (the prefill tile then holds two tokens, or one, of every
 head of the group), odd groups that do not divide the 128-row tile (7, and a
 single head), and decode groups that take several head chunks of 8, 4 or 1
 heads per CTA (24, 12, 7).  Every output row, every appended cache slot and
-every per-key probability is compared with the oracle."""
+every per-key probability is compared with the oracle.  Also caches smaller
+than one key tile (1 to 130 slots), where a tile reaches into the next
+sequence's slab or past the cache."""
 import numpy as np
 import pytest
 import torch
@@ -71,3 +73,38 @@ def test_decode_wide_and_odd_groups(oracle, name):
     for b, n in enumerate(dec.kv_lens.tolist()):
         assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"{name} probs b{b}")
         assert bool((probs[b, :, n:] == -7.0).all()), "probs written past kv_len"
+
+
+@pytest.mark.parametrize("cap,prior,new", [(40, [0, 10], [7, 30]), (1, [0, 0], [1, 1]),
+                                           (130, [1, 64], [128, 66])])
+def test_prefill_cache_smaller_than_a_key_tile(oracle, cap, prior, new):
+    """Capacities of 1, 40 and 130 slots: a 128-key tile reaches past a
+    sequence's slab into the next one's (or past the cache), and those rows
+    must be masked and zeroed, never attended."""
+    spec = W.Spec(H=4, KV=2, d=64, rd=64, out_gate=True)
+    step = W.make_step(spec, prior, new, cap, seed=47)
+    g = gpu_step(step)
+    assert g.status == 0, f"status {g.status}"
+    ost = oracle_append(oracle, step)
+    check_cache(g.cache_k, g.cache_v, step, ost)
+    rows = list(range(step.total_tokens))
+    ref = oracle_rows(oracle, step, ost, rows)
+    assert_out_close(g.out[rows].to(torch.float64).numpy(), ref, f"capacity {cap}")
+
+
+@pytest.mark.parametrize("cap,lens", [(40, [40, 1, 0, 17]), (1, [1, 1, 0]), (65, [65, 64, 3])])
+def test_decode_cache_smaller_than_a_key_tile(oracle, cap, lens):
+    """Decode over caches of 1, 40 and 65 slots (64-key tiles reach into the
+    next slab or past the cache)."""
+    s = W.Spec(H=8, KV=2, d=128, rd=128)
+    dec = W.make_decode(s, lens, cap, seed=49)
+    out, probs, status = gpu_decode(dec, with_probs=True)
+    assert status == 0
+    ref_out, ref_p = oracle.decode(
+        s.H, s.KV, s.d, score_scale(s), oracle_flags(s, False), W.bf16_to_f64(dec.q),
+        np.ascontiguousarray(W.bf16_to_f64(dec.cache_k)),
+        np.ascontiguousarray(W.bf16_to_f64(dec.cache_v)), dec.kv_lens.numpy(),
+        probs_stride=probs.shape[-1])
+    assert_out_close(out.double().numpy(), ref_out, f"capacity {cap} out")
+    for b, n in enumerate(lens):
+        assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"capacity {cap} probs b{b}")
