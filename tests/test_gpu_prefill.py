@@ -326,3 +326,54 @@ def test_full_varlen_step_b16_qknorm_gate(oracle):
         if cu[b + 1] > cu[b]:
             rows += [cu[b], cu[b + 1] - 1]
     _compare_step(oracle, step, rows=sorted(set(rows)), what="varlen full")
+
+
+def test_pair_equals_two_sequential_calls():
+    """The pages' pair test on the GPU: two drafted tokens per sequence in one
+    call against the same tokens in two one-token calls (append, attend, then
+    the next): the caches are bit-identical and every output row agrees within
+    the output tolerance (the two calls tile and split the keys differently)."""
+    import causal_gqa_attention_rope_gb300 as na
+    from harness import attn_cfg, rope_cfg
+    spec = W.Spec(H=32, KV=8, d=128, rd=128, qk_norm=True, out_gate=True,
+                  rope=W.RopeParams(base=5e5))
+    prior = [700, 64, 2048, 1]
+    B = len(prior)
+    step = W.make_step(spec, prior, [2] * B, 2176, seed=221)
+    dev = "cuda"
+    cfg, rope = attn_cfg(spec), rope_cfg(spec)
+    dv = lambda x: None if x is None else x.to(dev).contiguous()
+    qw, kw = dv(step.q_norm_w), dv(step.k_norm_w)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(cache, cu, lens, q, k, v, gate, n_max):
+        T = q.shape[0]
+        q_out, out = torch.empty_like(q), torch.empty_like(q)
+        na.na_rope_append_kv(cfg, rope, cu, lens, q, k, v, q_out, cache, q_norm_w=qw, k_norm_w=kw,
+                             status=st)
+        mt = int(lens.max()) + n_max
+        ws = na.workspace(na.na_prefill_workspace_size(cfg, B, T, n_max, mt), dev)
+        na.na_attn_prefill_chunk(cfg, cu, lens, n_max, mt, q_out, cache, out, gate=gate,
+                                 workspace=ws, status=st)
+        return out
+
+    # one call: both drafted tokens of every sequence
+    pair_cache = na.KVCache(dv(step.cache_k), dv(step.cache_v))
+    out_pair = run(pair_cache, dv(step.cu_seqlens), dv(step.cache_lens), dv(step.q), dv(step.k),
+                   dv(step.v), dv(step.gate), 2).cpu()
+    # two calls of one token per sequence
+    seq_cache = na.KVCache(dv(step.cache_k), dv(step.cache_v))
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    outs = []
+    for i in range(2):
+        pick = lambda x: x[i::2].contiguous().to(dev)  # token i of every sequence
+        lens = torch.tensor([p + i for p in prior], dtype=torch.int32, device=dev)
+        outs.append(run(seq_cache, cu1, lens, pick(step.q), pick(step.k), pick(step.v),
+                        pick(step.gate), 1).cpu())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(pair_cache.k.cpu().view(torch.int16), seq_cache.k.cpu().view(torch.int16))
+    assert torch.equal(pair_cache.v.cpu().view(torch.int16), seq_cache.v.cpu().view(torch.int16))
+    for i in range(2):
+        assert_out_close(out_pair[i::2].double().numpy(), outs[i].double().numpy(),
+                         f"drafted token {i}: pair against single calls")
