@@ -309,3 +309,31 @@ def test_calls_follow_the_current_stream(oracle):
     torch.cuda.synchronize()
     assert status == 0
     assert torch.equal(out, ref_out)
+
+
+def test_decode_many_sequences(oracle):
+    """700 sequences of 0..600 keys (more streams than CTAs: a slice spans
+    many short streams and many streams have a single piece); sampled
+    sequences against the oracle, every output row finite, every probability
+    row summing to 1."""
+    rng = np.random.default_rng(231)
+    lens = [int(x) for x in rng.integers(0, 601, 700)]
+    spec = W.Spec(H=8, KV=2, d=64, rd=64, out_gate=True)
+    dec = W.make_decode(spec, lens, 608, seed=233)
+    out, probs, status = gpu_decode(dec, with_probs=True)
+    assert status == 0
+    assert bool(torch.isfinite(out.float()).all())
+    for b, n in enumerate(lens):
+        if n:
+            mass = probs[b, :, :n].double().sum(-1)
+            assert torch.allclose(mass, torch.ones_like(mass), atol=1e-4), f"mass b{b}"
+        else:
+            assert bool((out[b] == 0).all())
+    idx = sorted(set(sample_rows(len(lens), 40, seed=235)))
+    sub = W.DecodeInputs(spec=spec, q=dec.q[idx], cache_k=dec.cache_k[idx], cache_v=dec.cache_v[idx],
+                         kv_lens=dec.kv_lens[idx], gate=dec.gate[idx])
+    ref_out, ref_p = _oracle_decode(oracle, sub, stride=probs.shape[-1])
+    assert_out_close(out[idx].double().numpy(), ref_out, "many sequences out")
+    for i, b in enumerate(idx):
+        n = lens[b]
+        assert_probs_close(probs[b, :, :n].numpy(), ref_p[i, :, :n], f"many sequences probs b{b}")
