@@ -377,3 +377,27 @@ def test_pair_equals_two_sequential_calls():
     for i in range(2):
         assert_out_close(out_pair[i::2].double().numpy(), outs[i].double().numpy(),
                          f"drafted token {i}: pair against single calls")
+
+
+def test_prefill_many_short_sequences(oracle):
+    """200 sequences of 0..20 new tokens over 0..2000 cached ones in one call
+    (many partly filled GQA-packed tiles; more than 32 sequences, so the slots
+    are not ranked): twelve sequences against the oracle, row by row and slot
+    by slot."""
+    rng = np.random.default_rng(241)
+    B = 200
+    prior = [int(x) for x in rng.integers(0, 2001, B)]
+    new = [int(x) for x in rng.integers(0, 21, B)]
+    spec = W.Spec(H=16, KV=4, d=128, rd=128, qk_norm=True, out_gate=True,
+                  rope=W.RopeParams(base=1e6))
+    step = W.make_step(spec, prior, new, 2048, seed=243)
+    g = gpu_step(step)
+    assert g.status == 0, f"status {g.status}"
+    assert bool(torch.isfinite(g.out.float()).all())
+    idx = sorted({int(np.argmax(new)), int(np.argmax(prior))} |
+                 {b for b in sample_rows(B, 10, seed=245) if new[b] > 0})
+    sub, rows = _sequences_of(step, idx)
+    ost = oracle_append(oracle, sub)
+    check_cache(g.cache_k[idx], g.cache_v[idx], sub, ost)
+    ref = oracle_rows(oracle, sub, ost, list(range(sub.total_tokens)))
+    assert_out_close(g.out[rows].to(torch.float64).numpy(), ref, f"sequences {idx}")
