@@ -240,11 +240,15 @@ def test_decode_importance(oracle, stride):
     _check_importance(oracle, dec, probs_stride=stride)
 
 
-@pytest.mark.parametrize("H,stride", [(5, 1028), (3, 1031), (40, 1028)])
+@pytest.mark.parametrize("H,stride", [(5, 1028), (3, 1031), (40, 1028), (128, 1028),
+                                      (200, 1032), (256, 1028), (300, 1028)])
 def test_importance_head_counts(oracle, H, stride):
     """Importance alone, on given probabilities: head counts that do not split
-    evenly over the kernel's thread groups, ragged lengths around its 256-key
-    blocks, a scalar-path stride (not a multiple of 4) and accumulation."""
+    evenly over the load path's thread groups, ragged lengths around the
+    blocks, a stride that is not a multiple of 4 (load path), head counts that
+    shrink the tensor-map path's blocks to 128, 64 and 32 keys (40, 128,
+    200/256 heads), one past its 256-row box (300 heads: load path), and
+    accumulation."""
     gen = torch.Generator().manual_seed(H)
     lens = torch.tensor([0, 1, 255, 256, 257, 1027], dtype=torch.int32)
     B = lens.numel()
