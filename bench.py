@@ -801,6 +801,7 @@ def reference_arm(args, wl):
     line["cpu_baseline"] = cb
     line["e2e"] = {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     line["config"] = dict(line["config"], launch="CPU oracle, single thread")
+    line["dtype"] = "f64"  # the oracle's arithmetic (bf16 inputs widened exactly)
     return line
 
 
