@@ -658,9 +658,9 @@ __device__ __forceinline__ float prob_of(float raw, int j, int kf, float M, floa
 // row's raw scores as bulk copies into shared memory (two buffers of `half`
 // 16-byte groups, refilled in turn for long rows) while the warps load every
 // piece's (max, sum) and the first pieces' output rows; no registers are
-// spent on loads in flight, so many CTAs share an SM.  128 threads: 2048
-// CTAs of one decode step fit in about one wave (256-thread CTAs were held
-// to six per SM by registers and took 1% longer per decode call).
+// spent on loads in flight, so many CTAs share an SM (six, held there by the
+// two 16 KB buffers).  128 threads: 256-thread CTAs took 1% longer per
+// decode call.
 constexpr int kCombThreads = 128;
 constexpr int kCombMaxHalf = 1024;  // 16-byte groups per buffer (4096 keys)
 
