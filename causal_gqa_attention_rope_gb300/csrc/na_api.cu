@@ -54,6 +54,25 @@ int check_cache(const na_kv_cache *cache, int batch)
 
 // The attention kernels address cache rows (sequence, kv head, slot) through
 // tensor maps whose row coordinate is a signed 32-bit integer.
+// The attention calls encode tensor maps with a driver call before they
+// launch, and a driver call needs the device's context current on the calling
+// thread.  The runtime binds it lazily (on a launch or a copy), so a thread
+// whose first CUDA call is one of these may not have it yet: the current
+// device's primary context is bound once per thread and device.
+int bind_context()
+{
+    thread_local int bound = -1;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NA_ERR_CUDA;
+    if (dev != bound) {
+        if (cudaSetDevice(dev) != cudaSuccess)
+            return NA_ERR_CUDA;
+        bound = dev;
+    }
+    return NA_OK;
+}
+
 int check_cache_rows(const na_kv_cache *cache, int kv_heads)
 {
     return (long long)cache->batch * kv_heads * cache->capacity > 0x7fffffffLL ? NA_ERR_UNSUPPORTED
@@ -389,6 +408,8 @@ int na_attn_prefill_chunk(const na_attn_cfg *cfg, int32_t batch, const int32_t *
         p.part_ml = p.part_o + (size_t)pl.tail_units * pl.num_splits * prefill_q_tile() * cfg->head_dim;
     }
     p.status = status;
+    if ((rc = bind_context()) != NA_OK)
+        return rc;
     return launch_prefill(p, cfg->head_dim, total_tokens, cache->batch,
                           static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
@@ -420,6 +441,8 @@ int na_decode_importance(const na_attn_cfg *cfg, int32_t batch, const float *pro
     p.kv_lens = kv_lens;
     p.imp = imp;
     p.status = status;
+    if ((rc = bind_context()) != NA_OK)
+        return rc;
     return launch_importance(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NA_OK
                                                                                    : NA_ERR_CUDA;
 }
@@ -499,6 +522,8 @@ int na_attn_decode(const na_attn_cfg *cfg, int32_t batch, const void *q_rot,
     p.part_ml = p.part_o + rows * cfg->head_dim;
     p.piece_span = reinterpret_cast<int32_t *>(p.part_ml + rows * 2);
     p.status = status;
+    if ((rc = bind_context()) != NA_OK)
+        return rc;
     return launch_decode(p, cfg->head_dim, pl.heads_per_cta, static_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? NA_OK

@@ -20,6 +20,10 @@
  *     workspace).  The library allocates no device memory, never synchronises
  *     the host with the device, and enqueues all work on `stream`
  *     (a cudaStream_t; NULL is the legacy default stream).
+ *   - Threads: calls may come from several host threads at once, each with its
+ *     own buffers, workspace and stream (na_attn_decode_static_ws excepted: its
+ *     calls share one scratch array).  Work goes to the calling thread's current
+ *     device, whose primary context the library makes current on that thread.
  *   - Errors: a negative na_status is returned when host-side validation fails;
  *     nothing is enqueued in that case.  Conditions only the device can see
  *     (a position past the cache capacity, an internal wait that timed out) are

@@ -203,3 +203,86 @@ def test_calls_on_two_streams_at_once():
         assert int(dst.item()) == 0 and int(pst.item()) == 0
         for a, b in zip(got, ref):
             assert torch.equal(_bits(a), _bits(b))
+
+
+def test_calls_from_several_host_threads():
+    """Four host threads, each with its own stream, workspace and buffers, call
+    the decode (two threads) and append + attend (two threads) ten times each
+    at once (the binding releases the interpreter lock inside the library):
+    every result equals the same call made alone."""
+    import threading
+
+    import causal_gqa_attention_rope_gb300 as na
+    dev = "cuda"
+
+    def make_decode_job(seed):
+        spec = W.Spec(H=16, KV=4, d=128, rd=128)
+        dec = W.make_decode(spec, [1500, 3, 777], 1536, seed=seed)
+        cfg = attn_cfg(spec)
+        q, kv = dec.q.to(dev), dec.kv_lens.to(dev)
+        cache = na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev))
+        out = torch.empty_like(q)
+        probs = torch.zeros(3, spec.H, 1500, device=dev)
+        ws = na.workspace(na.na_decode_workspace_size(cfg, 3, 1500), dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def run():
+            na.na_attn_decode(cfg, q, cache, kv, 1500, out, probs=probs, workspace=ws, status=st)
+            return [out, probs]
+        return run, st
+
+    def make_prefill_job(seed):
+        spec = W.Spec(H=8, KV=2, d=64, rd=64, qk_norm=True)
+        step = W.make_step(spec, [300, 0], [90, 40], 512, seed=seed)
+        cfg, rope = attn_cfg(spec), rope_cfg(spec)
+        cu, lens = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
+        q, k, v = (x.to(dev) for x in (step.q, step.k, step.v))
+        qw, kw = step.q_norm_w.to(dev), step.k_norm_w.to(dev)
+        ck0, cv0 = step.cache_k.to(dev), step.cache_v.to(dev)
+        cache = na.KVCache(ck0.clone(), cv0.clone())
+        q_out, out = torch.empty_like(q), torch.empty_like(q)
+        ws = na.workspace(na.na_prefill_workspace_size(cfg, 2, step.total_tokens, 90, 390), dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def run():
+            cache.k.copy_(ck0)
+            cache.v.copy_(cv0)
+            na.na_rope_append_kv(cfg, rope, cu, lens, q, k, v, q_out, cache, q_norm_w=qw,
+                                 k_norm_w=kw, status=st)
+            na.na_attn_prefill_chunk(cfg, cu, lens, 90, 390, q_out, cache, out, workspace=ws,
+                                     status=st)
+            return [out, q_out, cache.k, cache.v]
+        return run, st
+
+    jobs = [make_decode_job(301), make_decode_job(302), make_prefill_job(303),
+            make_prefill_job(304)]
+    refs = []
+    for run, _ in jobs:
+        refs.append([t.clone() for t in run()])
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        run, _ = jobs[i]
+        s = torch.cuda.Stream()
+        try:
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    got = run()
+                    s.synchronize()
+                    for a, b in zip(got, refs[i]):
+                        if not torch.equal(_bits(a), _bits(b)):
+                            errors.append(f"job {i} differs")
+                            return
+        except Exception as e:  # reported below
+            errors.append(f"job {i}: {e}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for _, st in jobs:
+        assert int(st.item()) == 0
