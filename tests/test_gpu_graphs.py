@@ -286,3 +286,50 @@ def test_calls_from_several_host_threads():
     assert not errors, errors
     for _, st in jobs:
         assert int(st.item()) == 0
+
+
+def test_first_call_of_a_thread_inside_graph_capture():
+    """A host thread whose very first library call is made while a CUDA graph
+    is being captured (a serving thread that captures its step at once): the
+    capture succeeds and its replay equals an eager call."""
+    import threading
+
+    import causal_gqa_attention_rope_gb300 as na
+    dev = "cuda"
+    spec = W.Spec(H=16, KV=4, d=128, rd=128)
+    dec = W.make_decode(spec, [900, 31], 1024, seed=311)
+    cfg = attn_cfg(spec)
+    q, kv = dec.q.to(dev), dec.kv_lens.to(dev)
+    cache = na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev))
+    out = torch.empty_like(q)
+    probs = torch.zeros(2, spec.H, 900, device=dev)
+    ws = na.workspace(na.na_decode_workspace_size(cfg, 2, 900), dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        na.na_attn_decode(cfg, q, cache, kv, 900, out, probs=probs, workspace=ws, status=st)
+
+    result = {}
+
+    def worker():
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            g.replay()
+            torch.cuda.synchronize()
+            result["graph"] = (out.clone(), probs.clone())
+        except Exception as e:  # reported below
+            result["error"] = repr(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "error" not in result, result.get("error")
+    out.zero_()
+    probs.zero_()
+    call()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(_bits(result["graph"][0]), _bits(out))
+    assert torch.equal(_bits(result["graph"][1]), _bits(probs))
