@@ -197,6 +197,31 @@ def _stream(stream) -> Optional[int]:
     return _current_stream()
 
 
+def _want(t, name: str, dtype: str, shape=None, min_rows: int = 0):
+    """A tensor's dtype and shape, checked before its pointer crosses the C ABI
+    (the library sees only pointers: a wrong dtype would be read as another
+    type, a short tensor past its end).  `shape` entries of None match any
+    size; the first dimension must also hold at least `min_rows`."""
+    if t is None:
+        return
+    import torch
+    if t.dtype != getattr(torch, dtype):
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None:
+        ok = t.dim() == len(shape) and all(w is None or int(t.shape[i]) == w
+                                           for i, w in enumerate(shape))
+        if not ok:
+            want = "[" + ", ".join("*" if w is None else str(w) for w in shape) + "]"
+            raise ValueError(f"{name}: expected shape {want}, got {list(t.shape)}")
+        if int(t.shape[0]) < min_rows:
+            raise ValueError(f"{name}: {int(t.shape[0])} rows, at least {min_rows} needed")
+
+
+def _want_cache(cache: "KVCache", cfg: "AttnConfig", batch: int):
+    _want(cache.k, "cache.k", "bfloat16", (None, cfg.num_kv_heads, None, cfg.head_dim), batch)
+    _want(cache.v, "cache.v", "bfloat16", tuple(cache.k.shape))
+
+
 def _check(fn: str, rc: int):
     if rc != NA_OK:
         raise NAError(fn, rc)
@@ -210,6 +235,17 @@ def na_rope_append_kv(cfg: AttnConfig, rope: RopeConfig, cu_seqlens, cache_lens,
     lib = load_library()
     T = int(q.shape[0]) if total_tokens is None else int(total_tokens)
     batch = int(cu_seqlens.numel()) - 1
+    H, KV, d = cfg.num_heads, cfg.num_kv_heads, cfg.head_dim
+    _want(cu_seqlens, "cu_seqlens", "int32", (None,))
+    _want(cache_lens, "cache_lens", "int32", (None,), batch)
+    _want(q, "q", "bfloat16", (None, H, d), T)
+    _want(q_out, "q_out", "bfloat16", (None, H, d), T)
+    _want(k, "k", "bfloat16", (None, KV, d), T)
+    _want(v, "v", "bfloat16", (None, KV, d), T)
+    _want(q_norm_w, "q_norm_w", "bfloat16", (d,))
+    _want(k_norm_w, "k_norm_w", "bfloat16", (d,))
+    _want(status, "status", "int32", (None,), 1)
+    _want_cache(cache, cfg, batch)
     c, r, kc = cfg.c(), rope.c(), cache.c()
     rc = lib.na_rope_append_kv(ctypes.byref(c), ctypes.byref(r), batch, _ptr(cu_seqlens),
                                _ptr(cache_lens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w),
@@ -247,6 +283,14 @@ def na_attn_prefill_chunk(cfg: AttnConfig, cu_seqlens, cache_lens, max_new_len: 
     lib = load_library()
     T = int(q_rot.shape[0]) if total_tokens is None else int(total_tokens)
     batch = int(cu_seqlens.numel()) - 1
+    H, d = cfg.num_heads, cfg.head_dim
+    _want(cu_seqlens, "cu_seqlens", "int32", (None,))
+    _want(cache_lens, "cache_lens", "int32", (None,), batch)
+    _want(q_rot, "q_rot", "bfloat16", (None, H, d), T)
+    _want(out, "out", "bfloat16", (None, H, d), T)
+    _want(gate, "gate", "bfloat16", (None, H, d), T)
+    _want(status, "status", "int32", (None,), 1)
+    _want_cache(cache, cfg, batch)
     c, kc = cfg.c(), cache.c()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.na_attn_prefill_chunk(ctypes.byref(c), batch, _ptr(cu_seqlens), _ptr(cache_lens), T,
@@ -256,11 +300,24 @@ def na_attn_prefill_chunk(cfg: AttnConfig, cu_seqlens, cache_lens, max_new_len: 
     _check("na_attn_prefill_chunk", rc)
 
 
+def _want_decode(cfg, q_rot, cache, kv_lens, out, probs, gate, status):
+    H, d = cfg.num_heads, cfg.head_dim
+    _want(q_rot, "q_rot", "bfloat16", (None, H, d))
+    B = int(q_rot.shape[0])
+    _want(out, "out", "bfloat16", (B, H, d))
+    _want(gate, "gate", "bfloat16", (B, H, d))
+    _want(kv_lens, "kv_lens", "int32", (None,), B)
+    _want(probs, "probs", "float32", (B, H, None))
+    _want(status, "status", "int32", (None,), 1)
+    _want_cache(cache, cfg, B)
+
+
 def na_attn_decode(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, max_kv_len: int, out,
                    probs=None, gate=None, workspace=None, num_splits: int = 0, status=None,
                    stream=None):
     lib = load_library()
     batch = int(q_rot.shape[0])
+    _want_decode(cfg, q_rot, cache, kv_lens, out, probs, gate, status)
     c, kc = cfg.c(), cache.c()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     stride = int(probs.shape[-1]) if probs is not None else 0
@@ -279,6 +336,7 @@ def na_attn_decode_static_ws(cfg: AttnConfig, q_rot, cache: KVCache, kv_lens, ma
     allocate device memory.  Calls that overlap on the GPU race on that array."""
     lib = load_library()
     batch = int(q_rot.shape[0])
+    _want_decode(cfg, q_rot, cache, kv_lens, out, probs, gate, status)
     c, kc = cfg.c(), cache.c()
     stride = int(probs.shape[-1]) if probs is not None else 0
     rc = lib.na_attn_decode_static_ws(ctypes.byref(c), batch, _ptr(q_rot), ctypes.byref(kc),
@@ -293,6 +351,11 @@ def na_decode_importance(cfg: AttnConfig, probs, kv_lens, max_kv_len: int, imp,
     """Born-rule importance of a decode step: imp[b][j] (+)= sum over heads of
     probs[b][h][j] for j < kv_lens[b].  probs [B,H,stride] fp32, imp [B,stride2]."""
     lib = load_library()
+    _want(probs, "probs", "float32", (None, cfg.num_heads, None))
+    B = int(probs.shape[0])
+    _want(imp, "imp", "float32", (B, None))
+    _want(kv_lens, "kv_lens", "int32", (None,), B)
+    _want(status, "status", "int32", (None,), 1)
     c = cfg.c()
     rc = lib.na_decode_importance(ctypes.byref(c), int(probs.shape[0]), _ptr(probs),
                                   int(probs.shape[-1]), _ptr(kv_lens), int(max_kv_len), _ptr(imp),

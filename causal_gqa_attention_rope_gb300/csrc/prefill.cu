@@ -257,7 +257,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (nsplit > 1)
         k_end = min(k_end, k_begin + p.split_len);
     bool run = true;  // uniform over the CTA
-    if (n_new > p.max_new_len || (b == 0 && tok0 != 0)) {
+    // A sequence must lie inside the call's tokens (cu_seqlens within
+    // [0, total_tokens]): its rows are read from Q and written to out.
+    if (n_new > p.max_new_len || (b == 0 && tok0 != 0) || tok0 < 0 ||
+        (long long)tok0 + n_new > p.total_tokens) {
         if (qt == 0 && hg == 0 && split == 0 && threadIdx.x == 0)
             na_report(p.status, NA_ERR_INVALID_ARG);
         run = false;
@@ -791,7 +794,8 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillParam
     slot_sequence(p, slot, lane, b, tok0, n_new, prior);
     const int r0 = qt * p.tile_tokens;
     const bool ring = (p.flags & NA_RING_CACHE) != 0;
-    if (n_new > p.max_new_len || (b == 0 && tok0 != 0) || r0 >= n_new)
+    if (n_new > p.max_new_len || (b == 0 && tok0 != 0) || tok0 < 0 ||
+        (long long)tok0 + n_new > p.total_tokens || r0 >= n_new)
         return;  // invalid bounds were reported by the attention pass
     const int rows_tok = min(p.tile_tokens, n_new - r0);
     const int pos_lo = prior + r0, pos_hi = pos_lo + rows_tok - 1;

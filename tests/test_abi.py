@@ -220,3 +220,47 @@ def test_no_fallback_for_cpu_tensors(lib):
     kv = torch.ones(1, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA tensors only"):
         na.na_attn_decode(cfg, q, cache, kv, 1, torch.empty_like(q))
+
+
+def test_binding_checks_dtypes_and_shapes(lib):
+    """The binding checks each tensor's dtype and shape against the config
+    before its pointer crosses the C ABI (the library sees pointers only):
+    a wrong dtype, a wrong head count or head dim, too few rows or a cache of
+    the wrong layout raise ValueError, before any CUDA work."""
+    import torch
+    bf = dict(dtype=torch.bfloat16)
+    cfg = na.AttnConfig(4, 2, 64)
+    cache = na.KVCache(torch.zeros(2, 2, 8, 64, **bf), torch.zeros(2, 2, 8, 64, **bf))
+    q = torch.zeros(2, 4, 64, **bf)
+    kv = torch.ones(2, dtype=torch.int32)
+    cases = [
+        (lambda: na.na_attn_decode(cfg, q.float(), cache, kv, 1, q), "q_rot: expected bfloat16"),
+        (lambda: na.na_attn_decode(cfg, torch.zeros(2, 3, 64, **bf), cache, kv, 1, q),
+         "q_rot: expected shape"),
+        (lambda: na.na_attn_decode(cfg, q, cache, kv.long(), 1, q), "kv_lens: expected int32"),
+        (lambda: na.na_attn_decode(cfg, q, cache, kv[:1], 1, q), "kv_lens: 1 rows"),
+        (lambda: na.na_attn_decode(cfg, q, cache, kv, 1, q, probs=torch.zeros(2, 4, 8)[:, :3]),
+         "probs: expected shape"),
+        (lambda: na.na_attn_decode(cfg, q, na.KVCache(cache.k, cache.v[:, :, :4]), kv, 1, q),
+         "cache.v: expected shape"),
+        (lambda: na.na_attn_decode(cfg, q, na.KVCache(torch.zeros(2, 2, 8, 32, **bf),
+                                                      torch.zeros(2, 2, 8, 32, **bf)), kv, 1, q),
+         "cache.k: expected shape"),
+        (lambda: na.na_rope_append_kv(cfg, na.RopeConfig(), torch.tensor([0, 3], dtype=torch.int32),
+                                      torch.zeros(1, dtype=torch.int32), q, torch.zeros(3, 2, 64, **bf),
+                                      torch.zeros(3, 2, 64, **bf), q, cache, total_tokens=3),
+         "q: 2 rows, at least 3 needed"),
+        (lambda: na.na_attn_prefill_chunk(cfg, torch.tensor([0, 2], dtype=torch.int32),
+                                          torch.zeros(1, dtype=torch.int32), 2, 2, q, cache, q,
+                                          gate=torch.zeros(2, 4, 64)), "gate: expected bfloat16"),
+        (lambda: na.na_decode_importance(cfg, torch.zeros(2, 4, 8), kv, 8,
+                                         torch.zeros(2, 8, dtype=torch.float64)),
+         "imp: expected float32"),
+    ]
+    for call, msg in cases:
+        with pytest.raises(ValueError, match=msg):
+            call()
+    # right dtypes and shapes: refused only for being CPU tensors
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        na.na_attn_decode(cfg, q, cache, kv, 1, torch.empty_like(q),
+                          probs=torch.zeros(2, 4, 8))

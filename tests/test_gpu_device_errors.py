@@ -139,3 +139,37 @@ def test_decode_length_past_max_kv_len(oracle):
         err = float(np.max(np.abs(imp[b, :n].double().numpy() - ref_imp[i, :n]))) if n else 0.0
         assert err <= spec.H * 1e-4, f"importance b{b}: {err:.3e}"
         assert torch.equal(imp[b, n:], init[b, n:])
+
+
+def test_prefill_sequence_past_total_tokens(oracle):
+    """cu_seqlens says 12 tokens while the call's total_tokens is 10: the
+    second sequence (tokens 5..11) would reach past Q and out, so it is
+    skipped and NA_ERR_INVALID_ARG written; the first is attended as usual and
+    nothing is written outside out's 10 rows (its guard bands intact)."""
+    import causal_gqa_attention_rope_gb300 as na
+    spec = W.Spec(H=4, KV=2, d=64, rd=64)
+    step = W.make_step(spec, [30, 8], [5, 7], 64, seed=77)
+    dev = "cuda"
+    cfg, rope = attn_cfg(spec), rope_cfg(spec)
+    cu, lens = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
+    cache = na.KVCache(step.cache_k.to(dev), step.cache_v.to(dev))
+    q = step.q.to(dev)
+    q_out = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    na.na_rope_append_kv(cfg, rope, cu, lens, q, step.k.to(dev), step.v.to(dev), q_out, cache,
+                         status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    T = 10
+    go = Guarded((T, spec.H, spec.d), torch.bfloat16, dev, fill=FILL)
+    ws = na.workspace(na.na_prefill_workspace_size(cfg, 2, T, 7, 38), dev)
+    na.na_attn_prefill_chunk(cfg, cu, lens, 7, 38, q_out[:T], cache, go.t, workspace=ws,
+                             status=st, total_tokens=T)
+    torch.cuda.synchronize()
+    go.check("out")
+    assert int(st.item()) == na.NA_ERR_INVALID_ARG
+    out = go.t.cpu()
+    ost = oracle_append(oracle, step)
+    ref = oracle_rows(oracle, step, ost, list(range(5)))
+    assert_out_close(out[:5].to(torch.float64).numpy(), ref, "first sequence")
+    assert bool((out[5:] == FILL).all()), "the skipped sequence's rows were written"

@@ -81,9 +81,10 @@ def test_zero_tokens_is_noop():
     k = W.sentinel_fill((1, 2, 8, 64)).to(dev)
     cache = na.KVCache(k, k.clone())
     e = torch.empty(0, 4, 64, dtype=torch.bfloat16, device=dev)
+    ekv = torch.empty(0, 2, 64, dtype=torch.bfloat16, device=dev)
     na.na_rope_append_kv(attn_cfg(spec), rope_cfg(spec), torch.zeros(2, dtype=torch.int32,
                                                                       device=dev),
-                         torch.zeros(1, dtype=torch.int32, device=dev), e, e, e, e, cache,
+                         torch.zeros(1, dtype=torch.int32, device=dev), e, ekv, ekv, e, cache,
                          total_tokens=0)
     torch.cuda.synchronize()
     assert torch.equal(cache.k.cpu().view(torch.int16), k.cpu().view(torch.int16))
