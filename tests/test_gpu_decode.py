@@ -341,3 +341,26 @@ def test_decode_many_sequences(oracle):
     for i, b in enumerate(idx):
         n = lens[b]
         assert_probs_close(probs[b, :, :n].numpy(), ref_p[i, :, :n], f"many sequences probs b{b}")
+
+
+@pytest.mark.parametrize("H,stride,lens", [(8, 40, [0, 1, 39, 40]), (32, 4, [4, 3, 1]),
+                                           (4, 260, [259, 260, 7])])
+def test_importance_short_strides(oracle, H, stride, lens):
+    """Probability rows shorter than one 256-key block (40 and 4 keys) and
+    just over one (260): the tensor-map path's box reaches past the rows (or
+    the call takes the load path); every key against the oracle."""
+    gen = torch.Generator().manual_seed(stride)
+    kv = torch.tensor(lens, dtype=torch.int32)
+    B = kv.numel()
+    probs = torch.rand((B, H, stride), generator=gen, dtype=torch.float32)
+    init = torch.rand((B, stride), generator=gen, dtype=torch.float32)
+    dec = W.DecodeInputs(spec=W.Spec(H=H, KV=1, d=64, rd=64), q=None, cache_k=None,
+                         cache_v=None, kv_lens=kv, gate=None)
+    got, st = _gpu_importance(dec, probs, init, True)
+    assert st == 0
+    ref = oracle.decode_importance(H, probs.double().numpy(), kv.numpy(),
+                                   imp=init.double().numpy(), accumulate=True)
+    for b, n in enumerate(lens):
+        err = float(np.max(np.abs(got[b, :n].double().numpy() - ref[b, :n]))) if n else 0.0
+        assert err <= H * (H + 1) * 2.0 ** -24, f"importance b{b}: {err:.3e}"
+        assert torch.equal(got[b, n:], init[b, n:])
