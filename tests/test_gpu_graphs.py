@@ -333,3 +333,57 @@ def test_first_call_of_a_thread_inside_graph_capture():
     assert int(st.item()) == 0
     assert torch.equal(_bits(result["graph"][0]), _bits(out))
     assert torch.equal(_bits(result["graph"][1]), _bits(probs))
+
+
+@pytest.mark.parametrize("first", ["prefill", "importance"])
+def test_first_call_of_a_thread(first):
+    """A fresh host thread whose first library call is the attention call (no
+    append before it on that thread) or the importance pass: both encode
+    tensor maps before they launch, and must bind the device's context first.
+    The results equal the same call made on the main thread."""
+    import threading
+
+    import causal_gqa_attention_rope_gb300 as na
+    dev = "cuda"
+    if first == "prefill":
+        spec = W.Spec(H=8, KV=2, d=128, rd=128)
+        step = W.make_step(spec, [200, 0], [64, 30], 512, seed=321)
+        cfg, rope = attn_cfg(spec), rope_cfg(spec)
+        cu, lens = step.cu_seqlens.to(dev), step.cache_lens.to(dev)
+        cache = na.KVCache(step.cache_k.to(dev), step.cache_v.to(dev))
+        q_rot = torch.empty_like(step.q, device=dev)
+        na.na_rope_append_kv(cfg, rope, cu, lens, step.q.to(dev), step.k.to(dev),
+                             step.v.to(dev), q_rot, cache)
+        out = torch.empty_like(q_rot)
+        ws = na.workspace(na.na_prefill_workspace_size(cfg, 2, step.total_tokens, 64, 264), dev)
+
+        def call():
+            na.na_attn_prefill_chunk(cfg, cu, lens, 64, 264, q_rot, cache, out, workspace=ws)
+            return out
+    else:
+        cfg = attn_cfg(W.Spec(H=16, KV=4, d=128, rd=128))
+        gen = torch.Generator().manual_seed(323)
+        probs = torch.rand((3, 16, 2048), generator=gen).to(dev)
+        kv = torch.tensor([2048, 5, 1000], dtype=torch.int32, device=dev)
+        imp = torch.zeros(3, 2048, device=dev)
+
+        def call():  # overwrites imp (no accumulation): no torch op before it
+            na.na_decode_importance(cfg, probs, kv, 2048, imp)
+            return imp
+    torch.cuda.synchronize()
+    result = {}
+
+    def worker():
+        try:
+            result["got"] = call().clone()
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below
+            result["error"] = repr(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "error" not in result, result.get("error")
+    ref = call().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(result["got"]), _bits(ref))
