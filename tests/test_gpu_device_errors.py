@@ -173,3 +173,44 @@ def test_prefill_sequence_past_total_tokens(oracle):
     ref = oracle_rows(oracle, step, ost, list(range(5)))
     assert_out_close(out[:5].to(torch.float64).numpy(), ref, "first sequence")
     assert bool((out[5:] == FILL).all()), "the skipped sequence's rows were written"
+
+
+def test_loose_host_bounds(oracle):
+    """Host bounds far above the real lengths, as a serving loop that passes
+    its capacities: max_new_len 1024 for chunks of 100 and 30 tokens and
+    max_total_len 131072 over histories of 300 and 50 (the key ranges are cut
+    for a 131072-key span, so nearly every piece has no keys), and a decode
+    with max_kv_len 131072 over 20..700 keys: every row against the oracle."""
+    import causal_gqa_attention_rope_gb300 as na
+    spec = W.Spec(H=8, KV=2, d=128, rd=128, out_gate=True)
+    step = W.make_step(spec, [300, 50], [100, 30], 131072, seed=79)
+    out, ck, cv, sa, sb = _append_and_attend(step, max_new_len=1024, max_total_len=131072)
+    assert sa == 0 and sb == 0
+    ost = _check_rows(oracle, step, out, [0, 1], [], "loose bounds")
+    check_cache(ck, cv, step, ost)
+
+    dec = W.make_decode(spec, [700, 20, 333], 131072, seed=81)
+    dev, mx = "cuda", 131072
+    cfg = attn_cfg(spec)
+    q = dec.q.to(dev)
+    go = Guarded(q.shape, q.dtype, dev)
+    gp = Guarded((3, spec.H, mx), torch.float32, dev, fill=FILL)
+    ws = na.workspace(na.na_decode_workspace_size(cfg, 3, mx), dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    na.na_attn_decode(cfg, q, na.KVCache(dec.cache_k.to(dev), dec.cache_v.to(dev)),
+                      dec.kv_lens.to(dev), mx, go.t, probs=gp.t, gate=dec.gate.to(dev),
+                      workspace=ws, status=st)
+    torch.cuda.synchronize()
+    go.check("decode out")
+    gp.check("decode probs")
+    assert int(st.item()) == 0
+    ref_out, ref_p = oracle.decode(
+        spec.H, spec.KV, spec.d, score_scale(spec), oracle_flags(spec, False),
+        W.bf16_to_f64(dec.q), np.ascontiguousarray(W.bf16_to_f64(dec.cache_k[:, :, :700])),
+        np.ascontiguousarray(W.bf16_to_f64(dec.cache_v[:, :, :700])), dec.kv_lens.numpy(),
+        gate=W.bf16_to_f64(dec.gate), probs_stride=mx)
+    assert_out_close(go.t.cpu().double().numpy(), ref_out, "decode, loose bound")
+    probs = gp.t.cpu()
+    for b, n in enumerate([700, 20, 333]):
+        assert_probs_close(probs[b, :, :n].numpy(), ref_p[b, :, :n], f"probs b{b}")
+        assert bool((probs[b, :, n:] == FILL).all())
